@@ -1,0 +1,188 @@
+/*
+ * ws.h -- C ABI of the streaming block-causal hot path (B300, sm_103a).
+ *
+ * One streaming unit (about 160 ms of interleaved video-latent, audio and
+ * text tokens) is one attention block.  Per unit the path is:
+ *   1. ws_kv_append          append the unit's K/V slice to the full-history cache
+ *   2. ws_block_causal_attn  the unit's queries against the whole cache
+ *   3. ws_fm_euler_step      the flow-matching Euler update, once per solver step
+ * and, once per session, ws_block_causal_prefill over a whole token sequence.
+ *
+ * Sources (web pages about Wan-Streamer, cited by title and section):
+ *  [explainer]  Wan Streamer real-time AV explainer (xiaohu-jiedu.pages.dev),
+ *               "怎么做到边听边说、随时能打断" -- block-causal visibility;
+ *               "点开看部署细节" -- prefill, then the shared full-history cache.
+ *  [close-read] "全双工语音模型精读⑫：Wan-Streamer——当全双工长出一张脸"
+ *               (alwayszhang.cn), 3.2 -- flow-matching interpolant/velocity;
+ *               四、推理 steps 1-3 -- the performer appends the received KV
+ *               slice to its full-history cache, then runs the flow solver.
+ *  [youleyou]   "阿里通义万相发布亚秒级同步AI视频通话基础模型" (youleyou.com),
+ *               3.1 -- block-causal attention over the interleaved sequence;
+ *               3.3 -- the performer runs only the flow-matching solver.
+ *
+ * Conventions shared by every call
+ *  - Ownership: the caller owns every buffer; the library allocates no device
+ *    memory.  Scratch for split-KV attention is a caller-supplied workspace
+ *    sized by ws_block_causal_attn_workspace_size().
+ *  - Streams: every call is asynchronous on the caller's stream (NULL = the
+ *    legacy default stream) and never synchronises.
+ *  - Errors: every call returns a ws_status.  A call that fails validation
+ *    launches nothing and touches no memory.  ws_last_error() gives a
+ *    thread-local message for the last failure on the calling thread.
+ *  - Pointers marked "device" are device addresses.  Pointers marked "host"
+ *    are ordinary host memory read during the call only.
+ *  - Alignment: every device tensor pointer must be 16-byte aligned.
+ *  - Dtypes: WS_BF16 (bfloat16) or WS_F32 (float32).
+ */
+#ifndef WS_H_
+#define WS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define WS_API __attribute__((visibility("default")))
+#else
+#define WS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* ws_stream_t;
+
+typedef enum {
+  WS_OK = 0,
+  WS_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, bad offsets, misalignment */
+  WS_ERR_UNSUPPORTED = 2,      /* dtype / head_dim combination not implemented */
+  WS_ERR_CAPACITY = 3,         /* write or read past the cache capacity */
+  WS_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+  WS_ERR_TIMEOUT = 5           /* a bounded in-kernel wait gave up (device error word) */
+} ws_status;
+
+typedef enum { WS_F32 = 0, WS_BF16 = 1 } ws_dtype;
+
+/*
+ * ws_kv_append -- write one unit's K/V slice into the full-history cache.
+ * [close-read] 四、推理 step 3; [youleyou] 3.3.
+ *
+ *   k_cache[h][cache_len + t][:] = k_new[t][h][:]   (same for V)
+ *   for 0 <= t < n_new, 0 <= h < num_heads.  A bit copy; no other cache row
+ *   changes.
+ *
+ * k_new, v_new    device, [n_new][num_heads][head_dim], token-major, dtype dt
+ * k_cache, v_cache device, [num_heads][capacity][head_dim], dtype dt
+ * Requires 0 <= cache_len, n_new >= 0, cache_len + n_new <= capacity
+ * (else WS_ERR_CAPACITY), head_dim * sizeof(dt) a multiple of 16.
+ * n_new == 0 is a no-op.
+ */
+WS_API ws_status ws_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                       int64_t cache_len, int64_t n_new, int64_t capacity, int num_heads,
+                       int head_dim, ws_dtype dt, ws_stream_t stream);
+
+/*
+ * ws_block_causal_attn -- attention of the newest unit's tokens against the
+ * whole cache.  [explainer] "怎么做到边听边说": tokens see their own block in
+ * both directions and every earlier block, never a later one; [youleyou] 3.1.
+ *
+ * The blocks are given by offsets[0..n_blocks] (offsets[0] = 0,
+ * non-decreasing).  The query block is the last one, blk = n_blocks - 1,
+ * holding q_len = offsets[n_blocks] - offsets[n_blocks-1] tokens; the cache
+ * must already hold blocks 0..blk (append first, then attend).  Every query
+ * row therefore sees the keys j < kv_len = offsets[n_blocks]:
+ *
+ *   O[i][h] = sum_j softmax_j(s * <q[i][h], k[h][j]>) v[h][j],  j < kv_len
+ *   lse[h][i] = ln sum_j exp(s * <q[i][h], k[h][j]>)             (natural log)
+ *
+ * q           device, [q_len][num_heads][head_dim], dtype dt
+ * k_cache,
+ * v_cache     device, [num_heads][capacity][head_dim], dtype dt
+ * out         device, [q_len][num_heads][head_dim], dtype dt
+ * lse_or_null device float32 [num_heads][q_len], or NULL
+ * h_offsets   host int32 [n_blocks + 1] (validation and launch sizing)
+ * d_offsets   device int32 [n_blocks + 1], same values (read by kernels)
+ * softmax_scale  s > 0; 0 selects 1/sqrt(head_dim); negative is rejected
+ * workspace   device scratch of at least
+ *             ws_block_causal_attn_workspace_size(q_len, kv_len, num_heads,
+ *             head_dim) bytes (may be NULL when that size is 0); its contents
+ *             on entry do not matter; concurrent calls must not share it.
+ * Supported: (WS_BF16, head_dim 128) on tcgen05 tensor cores with fp32
+ * accumulation and bf16 P; (WS_F32, head_dim 64 or 128) on fp32 CUDA cores.
+ * Other combinations return WS_ERR_UNSUPPORTED.
+ */
+WS_API ws_status ws_block_causal_attn(const void* q, const void* k_cache, const void* v_cache, void* out,
+                               float* lse_or_null, const int32_t* h_offsets,
+                               const int32_t* d_offsets, int n_blocks, int64_t capacity,
+                               int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
+                               void* workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/*
+ * ws_block_causal_prefill -- full-sequence block-causal attention over all
+ * T = offsets[n_blocks] tokens (the session prefill before streaming;
+ * [explainer] "点开看部署细节").  Row i sees keys j < e(i), where e(i) is the
+ * end offset of the block holding token i.  Key tiles that no row of a query
+ * tile can see are skipped.
+ *
+ * q     device, [T][num_heads][head_dim]; out likewise; lse_or_null [H][T].
+ * Caches, offsets, scale, dtype rules and errors as ws_block_causal_attn.
+ * The prefill needs no workspace (pass NULL, 0).
+ */
+WS_API ws_status ws_block_causal_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                  void* out, float* lse_or_null, const int32_t* h_offsets,
+                                  const int32_t* d_offsets, int n_blocks, int64_t capacity,
+                                  int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
+                                  void* workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/*
+ * ws_fm_euler_step -- one Euler step of the flow-matching solver towards
+ * tau = 0.  [close-read] 3.2: z_tau = (1 - tau) z_0 + tau eps, velocity
+ * dz/dtau = eps - z_0; the step is  z <- z - dtau * v  (in place).
+ *
+ * z                  device, n_elems values of dtype z_dt (only WS_F32)
+ * v                  device, n_elems values of dtype v_dt (WS_BF16 or WS_F32)
+ * z_bf16_out_or_null device bf16 [n_elems], receives the updated z rounded to
+ *                    bf16 (the next network input), or NULL
+ * One fused multiply-add per element in fp32.  n_elems == 0 is a no-op.
+ */
+WS_API ws_status ws_fm_euler_step(void* z, ws_dtype z_dt, const void* v, ws_dtype v_dt,
+                           void* z_bf16_out_or_null, int64_t n_elems, float dtau,
+                           ws_stream_t stream);
+
+/*
+ * Bytes of workspace ws_block_causal_attn needs for these sizes on the
+ * current device (0 when no key range is split).  Returns SIZE_MAX when the
+ * sizes are invalid or the device cannot be queried.
+ */
+WS_API size_t ws_block_causal_attn_workspace_size(int64_t q_len, int64_t kv_len, int num_heads,
+                                           int head_dim);
+
+/* Static description of a status code. */
+WS_API const char* ws_status_string(ws_status s);
+
+/* Message of the last failed call on the calling thread ("" if none). */
+WS_API const char* ws_last_error(void);
+
+/*
+ * Device error word written by the attention kernels when a bounded wait
+ * gives up (they then stop, release their tensor memory and return).
+ * Synchronises the current device.  *code_out = 0 when clean; otherwise the
+ * call returns WS_ERR_TIMEOUT and *info_out says where (role << 8 | block).
+ */
+WS_API ws_status ws_get_device_error(int* code_out, int* info_out);
+WS_API ws_status ws_clear_device_error(void);
+
+/*
+ * Limit, in nanoseconds, of every in-kernel wait launched after this call
+ * (default 2e9).  Host-side setting, process wide.
+ */
+WS_API ws_status ws_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/* ABI version of this header (major * 100 + minor). */
+WS_API int ws_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WS_H_ */

@@ -1,0 +1,746 @@
+// attn_tcgen05.cu -- block-causal flash attention, bf16 in / fp32 accumulate,
+// head_dim 128, on sm_103a tensor cores (tcgen05 + TMEM + TMA + mbarrier).
+//
+// What it computes (Wan Streamer real-time AV explainer (xiaohu-jiedu.pages.dev),
+// "怎么做到边听边说、随时能打断"; "阿里通义万相发布亚秒级同步AI视频通话基础模型"
+// (youleyou.com), 3.1): query row i sees keys j < e(i), where e(i) is the end
+// offset of the block (streaming unit) holding token i -- its own block in both
+// directions, every earlier block, no later block.
+//   O_i = sum_{j<e(i)} softmax_j(s q_i.k_j) v_j,   LSE_i = ln sum_j exp(s q_i.k_j)
+//
+// CTA layout (one CTA per SM, 320 threads):
+//   warps 0-3  softmax for query tile 0 (thread = one query row)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q tiles once per work item, then K_j, V_j into a
+//              5-slot ring of 32 KB slots (128 rows x 128 cols, two 128-byte
+//              swizzled column halves)
+//   warp  9    TMEM owner and single-thread MMA issuer
+// TMEM (512 columns): tile t uses S_t = cols [256t, 256t+128) (fp32 logits,
+// overwritten in place by bf16 P in its first 64 columns) and
+// O_t = cols [256t+128, 256t+256) (fp32 output accumulator).
+//
+// Per key tile j, the MMA thread issues, in this order,
+//   PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j)
+// so that while one softmax group works on S_t(j) the tensor pipe has the
+// other tile's PV and QK queued.  tcgen05.mma instructions from one thread
+// execute in issue order, which orders QK_t(j) (writes S_t) after PV_t(j-1)
+// (reads P_t from the same columns).
+//
+// Softmax keeps a per-row running max m (log2 units of the scaled logits) and
+// sum l.  O is rescaled only when a row's max grows by more than 2^8 (lazy
+// rescale; exact after the final division by l).  P is rounded to bf16 before
+// PV.
+//
+// Work decomposition:
+//  * unit mode (the query block is the newest unit; every row sees all keys
+//    < kv_len): CTAs form `groups` of `pairs` CTAs; group g walks a contiguous
+//    range of the flattened (head, key tile) space and CTA p of the group
+//    holds query-tile pair p, so the CTAs of a group read the same K/V tiles at
+//    nearly the same time (one HBM read, L2 reuse).  A range that covers only
+//    part of a head writes a partial (O/l, log2-sum-exp) into the workspace;
+//    attn_combine_kernel merges the partials.
+//  * prefill mode: one work item per (head, query-tile pair), head-major,
+//    longest key range first; key tiles no row of a query tile can see are
+//    skipped; CTAs take items round-robin.
+//
+// Every wait is bounded (wall-clock limit): on time-out the kernel records an
+// error word, stops all roles, waits (bounded) for its own copies and MMAs in
+// flight, frees its tensor memory and returns.
+#include <cuda_bf16.h>
+
+#include "ws_internal.h"
+#include "ws_ptx.cuh"
+
+namespace ws {
+
+// Device error word: [0] code (0 = clean, 1 = wait time-out), [1] info.
+__device__ unsigned int g_attn_error[2];
+
+namespace {
+
+constexpr int BM = 128;                       // query rows per tile
+constexpr int BN = 128;                       // keys per tile
+constexpr int HD = 128;                       // head dim
+constexpr int NSTAGE = 5;                     // K/V ring slots
+constexpr int TILE_BYTES = BM * HD * 2;       // 32 KB
+constexpr int HALF_BYTES = TILE_BYTES / 2;    // 128 rows x 64 cols (128-byte rows)
+constexpr int NUM_THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr float LN2 = 0.69314718055994531f;
+// Teardown waits (copies / MMAs still in flight) never use a shorter limit.
+constexpr unsigned long long DRAIN_TIMEOUT_NS = 2000000000ull;
+
+// barrier indices
+constexpr int BAR_KV_FULL = 0;
+constexpr int BAR_KV_EMPTY = NSTAGE;
+constexpr int BAR_Q_FULL = 2 * NSTAGE;
+constexpr int BAR_Q_EMPTY = BAR_Q_FULL + 1;
+constexpr int BAR_S_FULL = BAR_Q_EMPTY + 1;   // [2]
+constexpr int BAR_P_FULL = BAR_S_FULL + 2;    // [2]
+constexpr int BAR_O_FULL = BAR_P_FULL + 2;    // [2]
+constexpr int BAR_O_FREE = BAR_O_FULL + 2;    // [2]
+constexpr int BAR_DRAIN = BAR_O_FREE + 2;
+constexpr int NUM_BARS = BAR_DRAIN + 1;
+
+constexpr int SMEM_Q = 0;
+constexpr int SMEM_KV = 2 * TILE_BYTES;
+constexpr int SMEM_BARS = SMEM_KV + NSTAGE * TILE_BYTES;
+constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;
+constexpr int SMEM_USED = SMEM_MISC + 16;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 B
+
+// wait sites (error info)
+enum : int { W_PROD_QE = 1, W_PROD_KVE, W_MMA_Q, W_MMA_KV, W_MMA_P, W_MMA_OF, W_SM_S, W_SM_O,
+             W_DRAIN_MMA, W_DRAIN_TMA };
+
+struct Params {
+  int prefill;
+  int heads, q_len, q_row0, kv_len, n_blocks;
+  int pairs, kv_tiles, groups;
+  long long work;
+  int n_items;
+  float scale_log2;
+  const int32_t* offs;
+  __nv_bfloat16* out;
+  float* lse;
+  float* ws_o;     // [grid*2][256][HD]
+  float* ws_lse;   // [grid*2][256]
+  unsigned long long timeout_ns;
+};
+
+struct Item {
+  int h, pair, t0;
+  int n[2];        // key tiles for query tile 0 / 1 (0: tile has no rows)
+  int slot;        // -1 final output, else partial slot 0/1
+};
+
+struct ItemIter {
+  long long f, fb, fe;
+  int p, i;
+};
+
+__device__ __forceinline__ int row_limit_dev(const int32_t* offs, int n_blocks, int token) {
+  int lo = 0, hi = n_blocks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(offs + mid) <= token) lo = mid;
+    else hi = mid - 1;
+  }
+  return __ldg(offs + lo + 1);
+}
+
+__device__ __forceinline__ void iter_init(const Params& P, ItemIter& it) {
+  if (!P.prefill) {
+    const int g = blockIdx.x / P.pairs;
+    it.p = blockIdx.x % P.pairs;
+    it.fb = static_cast<long long>(g) * P.work / P.groups;
+    it.fe = static_cast<long long>(g + 1) * P.work / P.groups;
+    it.f = it.fb;
+  } else {
+    it.i = blockIdx.x;
+  }
+}
+
+__device__ __forceinline__ bool iter_next(const Params& P, ItemIter& it, Item& item) {
+  if (!P.prefill) {
+    if (it.f >= it.fe) return false;
+    const int h = static_cast<int>(it.f / P.kv_tiles);
+    const int t0 = static_cast<int>(it.f % P.kv_tiles);
+    const long long rem = it.fe - it.f;
+    const int t1 = static_cast<int>(rem < P.kv_tiles - t0 ? t0 + rem : P.kv_tiles);
+    item.h = h;
+    item.pair = it.p;
+    item.t0 = t0;
+    item.slot = (t0 == 0 && t1 == P.kv_tiles) ? -1
+                                              : (h == static_cast<int>(it.fb / P.kv_tiles) ? 0 : 1);
+    for (int t = 0; t < 2; ++t)
+      item.n[t] = ((2 * it.p + t) * BM < P.q_len) ? (t1 - t0) : 0;
+    it.f += t1 - t0;
+    return true;
+  }
+  if (it.i >= P.n_items) return false;
+  item.h = it.i / P.pairs;
+  item.pair = P.pairs - 1 - it.i % P.pairs;   // longest key range first
+  item.t0 = 0;
+  item.slot = -1;
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = (2 * item.pair + t) * BM;
+    if (r0 < P.q_len) {
+      const int last = min(r0 + BM, P.q_len) - 1;
+      const int e = row_limit_dev(P.offs, P.n_blocks, P.q_row0 + last);
+      item.n[t] = (e + BN - 1) / BN;
+    } else {
+      item.n[t] = 0;
+    }
+  }
+  it.i += gridDim.x;
+  return true;
+}
+
+__device__ __forceinline__ void record_error(int where) {
+  if (atomicCAS(&g_attn_error[0], 0u, 1u) == 0u)
+    g_attn_error[1] = (static_cast<unsigned>(where) << 16) | (blockIdx.x & 0xFFFFu);
+}
+
+// Bounded wait on an mbarrier phase (slow path).  Returns false on time-out
+// or when another role has already aborted the CTA.
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned long long timeout_ns, int where) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        record_error(where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned long long timeout_ns, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, abort_flag, timeout_ns, where);
+}
+
+struct Ring {
+  uint32_t stage = 0, phase = 0;
+  __device__ __forceinline__ void advance() {
+    if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+  }
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  const uint32_t sQ = sbase + SMEM_Q;
+  const uint32_t sKV = sbase + SMEM_KV;
+  const uint32_t sBar = sbase + SMEM_BARS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + SMEM_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + SMEM_MISC + 4);
+  auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(bar(BAR_KV_FULL + s), 1);
+      mbar_init(bar(BAR_KV_EMPTY + s), 1);
+    }
+    mbar_init(bar(BAR_Q_FULL), 1);
+    mbar_init(bar(BAR_Q_EMPTY), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(BAR_S_FULL + t), 1);
+      mbar_init(bar(BAR_P_FULL + t), 128);
+      mbar_init(bar(BAR_O_FULL + t), 1);
+      mbar_init(bar(BAR_O_FREE + t), 128);
+    }
+    mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      ItemIter it;
+      iter_init(P, it);
+      Item item;
+      Ring ring;
+      uint32_t q_phase = 0;
+      int issued = 0, q_issued = 0;
+      bool ok = true;
+      while (ok && iter_next(P, it, item)) {
+        if (!wait_bar(bar(BAR_Q_EMPTY), q_phase ^ 1u, abort_flag, P.timeout_ns, W_PROD_QE)) break;
+        q_phase ^= 1u;
+        ++q_issued;
+        const int ntiles = (item.n[1] > 0) ? 2 : 1;
+        mbar_arrive_expect_tx(bar(BAR_Q_FULL), ntiles * TILE_BYTES);
+        for (int t = 0; t < ntiles; ++t) {
+          const int row0 = (2 * item.pair + t) * BM;
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_2d(sQ + t * TILE_BYTES + hf * HALF_BYTES, &tm_q, bar(BAR_Q_FULL),
+                        item.h * HD + hf * 64, row0);
+        }
+        const int n_iter = max(item.n[0], item.n[1]);
+        for (int j = 0; j < n_iter && ok; ++j) {
+          const int kv0 = (item.t0 + j) * BN;
+          for (int which = 0; which < 2; ++which) {
+            if (!wait_bar(bar(BAR_KV_EMPTY + ring.stage), ring.phase ^ 1u, abort_flag,
+                          P.timeout_ns, W_PROD_KVE)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = bar(BAR_KV_FULL + ring.stage);
+            mbar_arrive_expect_tx(full, TILE_BYTES);
+            const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(sKV + ring.stage * TILE_BYTES + hf * HALF_BYTES, map, full, hf * 64, kv0,
+                          item.h);
+            ++issued;
+            ring.advance();
+          }
+        }
+      }
+      // Teardown: every copy this warp started must have landed before the
+      // CTA may exit.  The ring slots filled last (up to NSTAGE of them) and
+      // the last Q load are waited for with bounded waits; loads already
+      // consumed return at once.
+      volatile int no_abort = 0;
+      const int pend = issued < NSTAGE ? issued : NSTAGE;
+      Ring back = ring;
+      for (int k = 0; k < pend; ++k) {
+        if (back.stage == 0) { back.stage = NSTAGE - 1; back.phase ^= 1u; }
+        else --back.stage;
+        wait_bar(bar(BAR_KV_FULL + back.stage), back.phase, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_TMA);
+      }
+      if (q_issued > 0)
+        wait_bar(bar(BAR_Q_FULL), static_cast<uint32_t>(q_issued - 1) & 1u, &no_abort,
+                 DRAIN_TIMEOUT_NS, W_DRAIN_TMA);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, 0, 1);
+      ItemIter it;
+      iter_init(P, it);
+      Item item;
+      Ring ring;
+      uint32_t q_phase = 0;
+      uint32_t p_phase[2] = {0u, 0u};
+      uint32_t of_phase[2] = {0u, 0u};
+      bool ok = true;
+
+      auto issue_qk = [&](int t, uint32_t kslot) {
+        const uint32_t a0 = sQ + t * TILE_BYTES;
+        const uint32_t b0 = sKV + kslot * TILE_BYTES;
+        const uint32_t d = tmem + 256u * t;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
+          mma_ss(d, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024),
+                 IDESC_QK, k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+        const uint32_t b0 = sKV + vslot * TILE_BYTES;
+        const uint32_t d = tmem + 256u * t + 128u;
+        const uint32_t a = tmem + 256u * t;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          mma_ts(d, a + 8u * k, smem_desc_sw128(b0 + k * 16 * 128, HALF_BYTES, 1024), IDESC_PV,
+                 (acc || k > 0) ? 1u : 0u);
+        }
+      };
+
+      while (ok && iter_next(P, it, item)) {
+        const int n_iter = max(item.n[0], item.n[1]);
+        if (!wait_bar(bar(BAR_Q_FULL), q_phase, abort_flag, P.timeout_ns, W_MMA_Q)) break;
+        q_phase ^= 1u;
+        tc_fence_after();
+        // prologue: QK_t(0)
+        const uint32_t k0 = ring.stage;
+        if (!wait_bar(bar(BAR_KV_FULL + ring.stage), ring.phase, abort_flag, P.timeout_ns,
+                      W_MMA_KV)) break;
+        ring.advance();
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (item.n[t] > 0) {
+            issue_qk(t, k0);
+            mma_commit(bar(BAR_S_FULL + t));
+          }
+        }
+        mma_commit(bar(BAR_KV_EMPTY + k0));
+        if (n_iter == 1) mma_commit(bar(BAR_Q_EMPTY));
+
+        for (int jj = 0; jj < n_iter && ok; ++jj) {
+          const uint32_t vslot = ring.stage;
+          if (!wait_bar(bar(BAR_KV_FULL + ring.stage), ring.phase, abort_flag, P.timeout_ns,
+                        W_MMA_KV)) { ok = false; break; }
+          ring.advance();
+          tc_fence_after();
+          const bool more = jj + 1 < n_iter;
+          uint32_t kslot = 0, kphase = 0;
+          if (more) { kslot = ring.stage; kphase = ring.phase; ring.advance(); }
+          bool k_ready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (jj >= item.n[t]) continue;
+            if (!wait_bar(bar(BAR_P_FULL + t), p_phase[t], abort_flag, P.timeout_ns, W_MMA_P)) {
+              ok = false; break;
+            }
+            p_phase[t] ^= 1u;
+            if (jj == 0) {
+              if (!wait_bar(bar(BAR_O_FREE + t), of_phase[t] ^ 1u, abort_flag, P.timeout_ns,
+                            W_MMA_OF)) { ok = false; break; }
+              of_phase[t] ^= 1u;
+            }
+            tc_fence_after();
+            issue_pv(t, vslot, jj > 0);
+            if (jj + 1 < item.n[t]) {
+              if (!k_ready) {
+                if (!wait_bar(bar(BAR_KV_FULL + kslot), kphase, abort_flag, P.timeout_ns,
+                              W_MMA_KV)) { ok = false; break; }
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_qk(t, kslot);
+              mma_commit(bar(BAR_S_FULL + t));
+            } else {
+              mma_commit(bar(BAR_O_FULL + t));
+            }
+          }
+          if (!ok) break;
+          mma_commit(bar(BAR_KV_EMPTY + vslot));
+          if (more) mma_commit(bar(BAR_KV_EMPTY + kslot));
+          if (jj + 2 == n_iter) mma_commit(bar(BAR_Q_EMPTY));
+        }
+      }
+      // Teardown: all MMAs this thread issued must be complete before the
+      // tensor memory is released.
+      mma_commit(bar(BAR_DRAIN));
+      volatile int no_abort = 0;
+      wait_bar(bar(BAR_DRAIN), 0u, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_MMA);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int r_in_tile = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 256u * t;
+    const uint32_t tO = tS + 128u;
+    uint32_t s_phase = 0, o_phase = 0;
+    ItemIter it;
+    iter_init(P, it);
+    Item item;
+    bool ok = true;
+    while (ok && iter_next(P, it, item)) {
+      const int n = item.n[t];
+      if (n == 0) continue;
+      const int row = (2 * item.pair + t) * BM + r_in_tile;   // local query row
+      const bool valid = row < P.q_len;
+      const int e_row = (P.prefill && valid) ? row_limit_dev(P.offs, P.n_blocks, P.q_row0 + row)
+                                             : P.kv_len;
+      float m = -INFINITY, l = 0.f;
+      for (int jj = 0; jj < n; ++jj) {
+        const bool got = wait_bar(bar(BAR_S_FULL + t), s_phase, abort_flag, P.timeout_ns, W_SM_S);
+        if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+        s_phase ^= 1u;
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s[c]);
+        tmem_ld_wait_only();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
+
+        const int kv0 = (item.t0 + jj) * BN;
+        if (kv0 + BN > e_row) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (kv0 + 32 * c + i >= e_row) s[c][i] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          mx0 = fmaxf(mx0, __uint_as_float(s[0][i]));
+          mx1 = fmaxf(mx1, __uint_as_float(s[1][i]));
+          mx2 = fmaxf(mx2, __uint_as_float(s[2][i]));
+          mx3 = fmaxf(mx3, __uint_as_float(s[3][i]));
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * P.scale_log2;
+        const bool need = m_tile > m + RESCALE_LOG2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? m_tile : m;
+          const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+          if (jj > 0) {
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t o[16];
+              tmem_ld16(tO + 16u * c, o);
+              tmem_ld_wait16(o);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(tO + 16u * c, o);
+            }
+          }
+          l *= alpha;
+          m = m_new;
+        }
+        const float mb = (m == -INFINITY) ? 0.f : m;
+        const float sc = P.scale_log2;
+        float l0 = 0.f, l1 = 0.f;
+        // p = 2^(x - m); packed in place: bf16 pair k of chunk c overwrites
+        // s[c][k] (both sources s[c][2k], s[c][2k+1] are already consumed),
+        // then columns 16c..16c+15 of S_t receive P[32c .. 32c+31].
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * k]), sc, -mb));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * k + 1]), sc, -mb));
+            l0 += p0;
+            l1 += p1;
+            s[c][k] = pack_bf16x2(p0, p1);
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pk[k] = s[c][k];
+          tmem_st16(tS + 16u * c, pk);
+        }
+        l += l0 + l1;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_P_FULL + t));
+      }
+      if (!ok) break;
+      // ---- epilogue: O_t / l
+      const bool got = wait_bar(bar(BAR_O_FULL + t), o_phase, abort_flag, P.timeout_ns, W_SM_O);
+      if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+      o_phase ^= 1u;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const float lse2 = m + __log2f(l);
+      if (item.slot < 0) {
+        __nv_bfloat16* dst = P.out + (static_cast<size_t>(row) * P.heads + item.h) * HD;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32u * c, o);
+          tmem_ld_wait(o);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+              d4[q] = w;
+            }
+          }
+        }
+        if (valid && P.lse != nullptr)
+          P.lse[static_cast<size_t>(item.h) * P.q_len + row] = lse2 * LN2;
+      } else {
+        const size_t slot = static_cast<size_t>(blockIdx.x) * 2 + item.slot;
+        const size_t prow = slot * 256 + t * BM + r_in_tile;
+        float* dst = P.ws_o + prow * HD;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32u * c, o);
+          tmem_ld_wait(o);
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                  __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+          }
+        }
+        if (valid) P.ws_lse[prow] = lse2;
+      }
+      tc_fence_before();
+      mbar_arrive(bar(BAR_O_FREE + t));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+namespace {
+
+__device__ __forceinline__ long long group_begin(long long g, long long work, int groups) {
+  return g * work / groups;
+}
+
+// The group whose range holds flattened index f: the largest g with
+// group_begin(g) <= f.
+__device__ __forceinline__ int group_of(long long f, long long work, int groups) {
+  return static_cast<int>(((f + 1) * groups + work - 1) / work) - 1;
+}
+
+// Merge the partial results of the groups that share one head:
+//   LSE = log2 sum_s 2^{lse_s},  O = sum_s 2^{lse_s - LSE} O_s.
+// One warp per (query row, head); lane c holds columns 4c..4c+3.
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(Params P) {
+  const int h = blockIdx.y;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= P.q_len) return;
+  const long long L = P.kv_tiles;
+  const int g_lo = group_of(h * L, P.work, P.groups);
+  const int g_hi = group_of((h + 1) * L - 1, P.work, P.groups);
+  if (g_lo == g_hi) return;   // one group covered the head: final output already written
+  const int pair = row / 256;
+  const int r = row % 256;
+  float mx = -INFINITY;
+  for (int g = g_lo; g <= g_hi; ++g) {
+    const int slot = (h == static_cast<int>(group_begin(g, P.work, P.groups) / L)) ? 0 : 1;
+    const size_t prow = (static_cast<size_t>(g * P.pairs + pair) * 2 + slot) * 256 + r;
+    mx = fmaxf(mx, P.ws_lse[prow]);
+  }
+  float sum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int g = g_lo; g <= g_hi; ++g) {
+    const int slot = (h == static_cast<int>(group_begin(g, P.work, P.groups) / L)) ? 0 : 1;
+    const size_t prow = (static_cast<size_t>(g * P.pairs + pair) * 2 + slot) * 256 + r;
+    const float w = exp2f(P.ws_lse[prow] - mx);
+    sum += w;
+    const float4 o = reinterpret_cast<const float4*>(P.ws_o + prow * HD)[lane];
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+  }
+  const float inv = 1.f / sum;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(P.out + (static_cast<size_t>(row) * P.heads + h) * HD)[lane] = packed;
+  if (lane == 0 && P.lse != nullptr)
+    P.lse[static_cast<size_t>(h) * P.q_len + row] = (mx + log2f(sum)) * LN2;
+}
+
+long long host_group_of(long long f, long long work, int groups) {
+  return ((f + 1) * groups + work - 1) / work - 1;
+}
+
+}  // namespace
+
+bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0, int kv_len,
+                  int n_blocks, int num_sms) {
+  p = TcAttnPlan{};
+  p.prefill = prefill ? 1 : 0;
+  p.heads = heads;
+  p.q_len = q_len;
+  p.q_row0 = q_row0;
+  p.kv_len = kv_len;
+  p.n_blocks = n_blocks;
+  p.qtiles = (q_len + BM - 1) / BM;
+  p.pairs = (p.qtiles + 1) / 2;
+  p.kv_tiles = (kv_len + BN - 1) / BN;
+  if (q_len <= 0 || kv_len <= 0 || heads <= 0 || num_sms <= 0) return false;
+  if (prefill) {
+    const long long items = static_cast<long long>(heads) * p.pairs;
+    if (items > (1LL << 30)) return false;
+    p.n_items = static_cast<int>(items);
+    p.grid = p.n_items < num_sms ? p.n_items : num_sms;
+    p.split = false;
+    p.workspace_bytes = 0;
+    return true;
+  }
+  p.work = static_cast<long long>(heads) * p.kv_tiles;
+  long long g = num_sms / p.pairs;
+  if (g < 1) g = 1;
+  if (g > p.work) g = p.work;
+  p.groups = static_cast<int>(g);
+  const long long grid = g * p.pairs;
+  if (grid > (1LL << 30)) return false;
+  p.grid = static_cast<int>(grid);
+  p.split = false;
+  for (int h = 0; h < heads && !p.split; ++h) {
+    const long long lo = host_group_of(static_cast<long long>(h) * p.kv_tiles, p.work, p.groups);
+    const long long hi = host_group_of(static_cast<long long>(h + 1) * p.kv_tiles - 1, p.work, p.groups);
+    p.split = lo != hi;
+  }
+  p.workspace_bytes = p.split ? static_cast<size_t>(p.grid) * 2 * 256 * (HD + 1) * sizeof(float) : 0;
+  return true;
+}
+
+cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
+                                const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, uint64_t timeout_ns, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !attr_done[dev]) {
+    err = cudaFuncSetAttribute(attn_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_ALLOC);
+    if (err != cudaSuccess) return err;
+    attr_done[dev] = true;
+  }
+  Params P{};
+  P.prefill = plan.prefill;
+  P.heads = plan.heads;
+  P.q_len = plan.q_len;
+  P.q_row0 = plan.q_row0;
+  P.kv_len = plan.kv_len;
+  P.n_blocks = plan.n_blocks;
+  P.pairs = plan.pairs;
+  P.kv_tiles = plan.kv_tiles;
+  P.groups = plan.groups;
+  P.work = plan.work;
+  P.n_items = plan.n_items;
+  P.scale_log2 = a.scale * 1.4426950408889634f;
+  P.offs = a.offs;
+  P.out = static_cast<__nv_bfloat16*>(a.out);
+  P.lse = a.lse;
+  if (plan.split) {
+    P.ws_o = static_cast<float*>(a.workspace);
+    P.ws_lse = P.ws_o + static_cast<size_t>(plan.grid) * 2 * 256 * HD;
+  }
+  P.timeout_ns = timeout_ns;
+  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, P);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (plan.split) {
+    dim3 grid((plan.q_len + 7) / 8, plan.heads);
+    attn_combine_kernel<<<grid, 256, 0, s>>>(P);
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+cudaError_t read_attn_device_error(int* code, int* info) {
+  unsigned int h[2] = {0u, 0u};
+  cudaError_t err = cudaMemcpyFromSymbol(h, g_attn_error, sizeof(h));
+  if (err != cudaSuccess) return err;
+  *code = static_cast<int>(h[0]);
+  *info = static_cast<int>(h[1]);
+  return cudaSuccess;
+}
+
+cudaError_t clear_attn_device_error() {
+  const unsigned int z[2] = {0u, 0u};
+  return cudaMemcpyToSymbol(g_attn_error, z, sizeof(z));
+}
+
+}  // namespace ws

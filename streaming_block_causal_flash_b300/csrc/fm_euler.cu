@@ -1,0 +1,112 @@
+// fm_euler.cu -- one Euler step of the flow-matching solver, z <- z - dtau * v.
+//
+// Interpolant z_tau = (1 - tau) z_0 + tau eps with velocity eps - z_0
+// ("全双工语音模型精读⑫：Wan-Streamer" (alwayszhang.cn), 3.2); the solver walks
+// tau from 1 (noise) towards 0 (clean latent).  One fp32 FMA per element,
+// z in place, v in bf16 or fp32, optionally a bf16 copy of the new z for the
+// next network input.  Eight elements per thread step: 32 B of z, 16 B (bf16)
+// or 32 B (fp32) of v, 16 B of bf16 output.
+#include <cuda_bf16.h>
+
+#include "ws_internal.h"
+
+namespace ws {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+template <bool kVBf16, bool kOutBf16>
+__global__ void __launch_bounds__(kThreads)
+fm_euler_kernel(float* __restrict__ z, const void* __restrict__ v_raw,
+                __nv_bfloat16* __restrict__ zb, int64_t n, float dtau) {
+  const int64_t n8 = n / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  const float neg = -dtau;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n8; i += stride) {
+    float4 z0 = ld_f4(z + 8 * i);
+    float4 z1 = ld_f4(z + 8 * i + 4);
+    float vf[8];
+    if constexpr (kVBf16) {
+      const uint4 vv = reinterpret_cast<const uint4*>(v_raw)[i];
+      bf16x8_to_f32(vv, vf);
+    } else {
+      const float4 a = ld_f4(static_cast<const float*>(v_raw) + 8 * i);
+      const float4 b = ld_f4(static_cast<const float*>(v_raw) + 8 * i + 4);
+      vf[0] = a.x; vf[1] = a.y; vf[2] = a.z; vf[3] = a.w;
+      vf[4] = b.x; vf[5] = b.y; vf[6] = b.z; vf[7] = b.w;
+    }
+    z0.x = fmaf(neg, vf[0], z0.x);
+    z0.y = fmaf(neg, vf[1], z0.y);
+    z0.z = fmaf(neg, vf[2], z0.z);
+    z0.w = fmaf(neg, vf[3], z0.w);
+    z1.x = fmaf(neg, vf[4], z1.x);
+    z1.y = fmaf(neg, vf[5], z1.y);
+    z1.z = fmaf(neg, vf[6], z1.z);
+    z1.w = fmaf(neg, vf[7], z1.w);
+    reinterpret_cast<float4*>(z)[2 * i] = z0;
+    reinterpret_cast<float4*>(z)[2 * i + 1] = z1;
+    if constexpr (kOutBf16) {
+      uint4 o;
+      o.x = f32x2_to_bf16x2(z0.x, z0.y);
+      o.y = f32x2_to_bf16x2(z0.z, z0.w);
+      o.z = f32x2_to_bf16x2(z1.x, z1.y);
+      o.w = f32x2_to_bf16x2(z1.z, z1.w);
+      reinterpret_cast<uint4*>(zb)[i] = o;
+    }
+  }
+  // ragged tail (n not a multiple of 8): the first block finishes it
+  if (blockIdx.x == 0) {
+    for (int64_t j = n8 * 8 + threadIdx.x; j < n; j += kThreads) {
+      float vj;
+      if constexpr (kVBf16)
+        vj = __bfloat162float(static_cast<const __nv_bfloat16*>(v_raw)[j]);
+      else
+        vj = static_cast<const float*>(v_raw)[j];
+      const float zn = fmaf(neg, vj, z[j]);
+      z[j] = zn;
+      if constexpr (kOutBf16) zb[j] = __float2bfloat16_rn(zn);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fm_euler(float* z, const void* v, bool v_is_bf16, void* z_bf16_out,
+                            int64_t n, float dtau, int num_sms, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int64_t n8 = n / 8;
+  int64_t blocks = (n8 + kThreads - 1) / kThreads;
+  const int64_t cap_blocks = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap_blocks) blocks = cap_blocks;
+  if (blocks < 1) blocks = 1;
+  auto* zb = static_cast<__nv_bfloat16*>(z_bf16_out);
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (v_is_bf16) {
+    if (zb) fm_euler_kernel<true, true><<<g, kThreads, 0, s>>>(z, v, zb, n, dtau);
+    else    fm_euler_kernel<true, false><<<g, kThreads, 0, s>>>(z, v, zb, n, dtau);
+  } else {
+    if (zb) fm_euler_kernel<false, true><<<g, kThreads, 0, s>>>(z, v, zb, n, dtau);
+    else    fm_euler_kernel<false, false><<<g, kThreads, 0, s>>>(z, v, zb, n, dtau);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ws

@@ -1,0 +1,78 @@
+// ws_internal.h -- host-side launchers shared between the C-ABI layer
+// (ws_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ws {
+
+// ---- KV append (kv_append.cu)
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             int64_t cache_len, int64_t n_new, int64_t capacity, int heads,
+                             int row_bytes, int num_sms, cudaStream_t s);
+
+// ---- Flow-matching Euler step (fm_euler.cu)
+cudaError_t launch_fm_euler(float* z, const void* v, bool v_is_bf16, void* z_bf16_out,
+                            int64_t n, float dtau, int num_sms, cudaStream_t s);
+
+// ---- fp32 SIMT attention (attn_simt.cu)
+struct SimtAttnArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  float* lse;            // may be null
+  const int32_t* offs;   // device offsets
+  int n_blocks;
+  int q_len;
+  int q_row0;            // global token index of q row 0
+  int kv_len;            // keys visible to every row (unit mode)
+  int heads;
+  int head_dim;          // 64 or 128
+  int64_t capacity;
+  float scale;           // softmax scale (natural units)
+  bool prefill;          // per-row limits from offsets
+};
+cudaError_t launch_attn_simt_f32(const SimtAttnArgs& a, cudaStream_t s);
+
+// ---- bf16 tcgen05 attention (attn_tcgen05.cu)
+struct TcAttnPlan {
+  int prefill;       // 0: one query block vs. the cache (split-KV groups); 1: prefill
+  int heads;
+  int q_len;
+  int q_row0;
+  int kv_len;
+  int n_blocks;
+  int qtiles;        // ceil(q_len / 128)
+  int pairs;         // ceil(qtiles / 2): query-tile pairs per head (one CTA each)
+  int kv_tiles;      // ceil(kv_len / 128)
+  int groups;        // unit mode: CTA groups over the (head, key tile) space
+  int64_t work;      // unit mode: heads * kv_tiles
+  int n_items;       // prefill mode: heads * pairs
+  int grid;          // CTAs launched
+  bool split;        // unit mode: some head's key range spans several groups
+  size_t workspace_bytes;
+};
+// Fills the plan for the given sizes; returns false when the sizes do not fit.
+bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0, int kv_len,
+                  int n_blocks, int num_sms);
+
+struct TcAttnArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  void* out;
+  float* lse;            // may be null
+  const int32_t* offs;   // device offsets
+  int64_t capacity;
+  float scale;           // softmax scale (natural units)
+  void* workspace;
+};
+cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
+                                const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, uint64_t timeout_ns, cudaStream_t s);
+cudaError_t read_attn_device_error(int* code, int* info);
+cudaError_t clear_attn_device_error();
+
+}  // namespace ws

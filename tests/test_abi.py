@@ -1,0 +1,108 @@
+"""C-ABI library: builds, loads, exports every declared symbol, and rejects
+bad arguments on the host before any CUDA call (CPU only, no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from streaming_block_causal_flash_b300 import build as ws_build
+from streaming_block_causal_flash_b300 import ws
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ws_build.build()
+    return ws.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "ws.h")).read()
+    return sorted(set(re.findall(r"WS_API\s+[\w\s\*]+?\b(ws_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = declared_symbols()
+    for n in ["ws_kv_append", "ws_block_causal_attn", "ws_block_causal_prefill", "ws_fm_euler_step"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert names == sorted(ws.SIGNATURES), "binding and header disagree"
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.ws_status_string(0) == b"WS_OK"
+    assert lib.ws_status_string(5) == b"WS_ERR_TIMEOUT"
+    assert ws.ws_abi_version() == 100
+
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced by host validation
+
+
+def _offs(vals):
+    a = np.asarray(vals, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def test_kv_append_host_validation(lib):
+    # capacity overflow
+    st = lib.ws_kv_append(FAKE, FAKE, FAKE, FAKE, 10, 5, 12, 2, 128, ws.WS_BF16, None)
+    assert st == ws.WS_ERR_CAPACITY and b"capacity" in lib.ws_last_error()
+    # unknown dtype
+    assert lib.ws_kv_append(FAKE, FAKE, FAKE, FAKE, 0, 1, 8, 1, 64, 7, None) == ws.WS_ERR_INVALID_ARGUMENT
+    # misaligned pointer
+    assert lib.ws_kv_append(FAKE + 8, FAKE, FAKE, FAKE, 0, 1, 8, 1, 64, ws.WS_BF16, None) == \
+        ws.WS_ERR_INVALID_ARGUMENT
+    # row not a multiple of 16 bytes
+    assert lib.ws_kv_append(FAKE, FAKE, FAKE, FAKE, 0, 1, 8, 1, 4, ws.WS_BF16, None) == ws.WS_ERR_UNSUPPORTED
+    # n_new == 0 is a no-op that succeeds without touching the device
+    assert lib.ws_kv_append(0, 0, 0, 0, 3, 0, 8, 1, 128, ws.WS_BF16, None) == ws.WS_OK
+
+
+def _attn(lib, fn, offs_vals, cap=1024, H=2, D=128, dt=ws.WS_BF16, scale=0.0, ptr=FAKE):
+    arr, p = _offs(offs_vals)
+    return getattr(lib, fn)(ptr, FAKE, FAKE, FAKE, None, p, FAKE, len(arr) - 1, cap, H, D,
+                            scale, dt, None, 0, None)
+
+
+@pytest.mark.parametrize("fn", ["ws_block_causal_attn", "ws_block_causal_prefill"])
+def test_attention_host_validation(lib, fn):
+    assert _attn(lib, fn, [1, 5]) == ws.WS_ERR_INVALID_ARGUMENT            # offsets[0] != 0
+    assert _attn(lib, fn, [0, 5, 3]) == ws.WS_ERR_INVALID_ARGUMENT         # decreasing
+    assert _attn(lib, fn, [0, 600, 1200]) == ws.WS_ERR_CAPACITY            # past capacity
+    assert _attn(lib, fn, [0, 8], D=64) == ws.WS_ERR_UNSUPPORTED          # bf16 needs D=128
+    assert _attn(lib, fn, [0, 8], D=96, dt=ws.WS_F32) == ws.WS_ERR_UNSUPPORTED
+    assert _attn(lib, fn, [0, 8], scale=-1.0) == ws.WS_ERR_INVALID_ARGUMENT
+    assert _attn(lib, fn, [0, 8], ptr=FAKE + 4) == ws.WS_ERR_INVALID_ARGUMENT
+    assert _attn(lib, fn, [0, 8], ptr=0) == ws.WS_ERR_INVALID_ARGUMENT
+    arr, p = _offs([0, 8])
+    assert getattr(lib, fn)(FAKE, FAKE, FAKE, FAKE, None, p, FAKE, 0, 16, 1, 128, 0.0,
+                            ws.WS_BF16, None, 0, None) == ws.WS_ERR_INVALID_ARGUMENT
+
+
+def test_euler_host_validation(lib):
+    assert lib.ws_fm_euler_step(FAKE, ws.WS_BF16, FAKE, ws.WS_BF16, None, 8, 0.25, None) == ws.WS_ERR_UNSUPPORTED
+    assert lib.ws_fm_euler_step(FAKE, ws.WS_F32, FAKE + 4, ws.WS_BF16, None, 8, 0.25, None) == \
+        ws.WS_ERR_INVALID_ARGUMENT
+    assert lib.ws_fm_euler_step(FAKE, ws.WS_F32, FAKE, ws.WS_BF16, None, 8, float("inf"), None) == \
+        ws.WS_ERR_INVALID_ARGUMENT
+    assert lib.ws_fm_euler_step(0, ws.WS_F32, 0, ws.WS_BF16, None, 0, 0.25, None) == ws.WS_OK
+
+
+def test_timeout_setting_rejects_zero(lib):
+    assert lib.ws_set_wait_timeout_ns(0) == ws.WS_ERR_INVALID_ARGUMENT
+    assert lib.ws_set_wait_timeout_ns(2_000_000_000) == ws.WS_OK
+
+
+def test_binding_raises_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(ws, "_lib", None)
+    monkeypatch.setattr(ws, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        ws.load()
