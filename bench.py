@@ -1,0 +1,579 @@
+#!/usr/bin/env python3
+"""Benchmark of the streaming block-causal hot path on one B300 per rank.
+
+One step = one 160 ms streaming unit: append the unit's K/V slice to the
+full-history cache, block-causal attention of the unit's queries against the
+whole cache, then the flow-matching Euler steps over the unit's latents --
+every call through the C ABI (``streaming_block_causal_flash_b300.ws``).
+
+Prints ONE JSON line (rank 0).  ``value`` is the attention's algorithmic
+TFLOP/s over the whole step (4*D*H*sum_i e(i) per unit / step time) summed
+over ranks; ``ms_per_step`` is the time of one unit.  See ``--help``.
+
+  python bench.py [--gpus N --steps K --warmup W --workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from streaming_block_causal_flash_b300.inputs import WORKLOADS, Workload  # noqa: E402
+
+METRIC = "block-causal attn TFLOP/s & µs per 160ms streaming unit (1 B300, vs roofline)"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "unit_640x368"
+L2_BYTES = 126 * 1024 * 1024
+ATTN_SOURCE = os.path.join(ROOT, "streaming_block_causal_flash_b300", "csrc", "attn_tcgen05.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_tcgen05_unit_640x368_traffic.txt")
+
+
+# ----------------------------------------------------------------- plumbing
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[k for k, w in WORKLOADS.items() if w.dtype == "bf16" and not w.prefill])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-hbm", action="store_true", help="skip the append/Euler HBM measurement")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        if device is not None and torch.distributed.get_backend() == "nccl":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+def reduce_over_ranks(local_ms: float, local_flops: float, world: int, device="cpu"):
+    """(max step time over ranks, total work over ranks)."""
+    if world == 1:
+        return local_ms, local_flops
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    w = torch.tensor([local_flops], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(w, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(w.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the GPU is busy."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def source_digest(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, or None
+    when the kernel source changed since those counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != source_digest(ATTN_SOURCE):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------- the workload
+
+def attention_flops(offsets: np.ndarray, rows: np.ndarray, heads: int, head_dim: int) -> float:
+    """4*D*H*sum_i e(i): QK^T and PV over the visible keys of each query row."""
+    offs = np.asarray(offsets, dtype=np.int64)
+    blk = np.searchsorted(offs, rows, side="right") - 1
+    e = offs[blk + 1]
+    return 4.0 * head_dim * heads * float(e.sum())
+
+
+class UnitSession:
+    """Device state for streaming units of one workload: the full-history
+    cache (history units resident), and per-unit inputs."""
+
+    def __init__(self, w: Workload, device, host_only=False):
+        self.w = w
+        self.sizes = w.unit_sizes()
+        self.offsets_all = w.offsets()
+        self.cap = w.capacity()
+        H, D = w.heads, w.head_dim
+        T_hist = int(self.offsets_all[w.history_units])
+        k = torch.zeros(H, self.cap, D, dtype=torch.bfloat16)
+        v = torch.zeros(H, self.cap, D, dtype=torch.bfloat16)
+        for h in range(H):
+            if w.history_units:
+                k[h, :T_hist] = w.head_timeline("k", h, w.history_units, self.sizes)
+                v[h, :T_hist] = w.head_timeline("v", h, w.history_units, self.sizes)
+        self.k_host, self.v_host = k, v
+        self.units = list(range(w.history_units, w.n_units))
+        # per new unit: Q, KV slice, velocities, eps
+        self.q_host = {u: w.token_major("q", u, self.sizes) for u in self.units}
+        self.kv_host = {u: (w.token_major("k", u, self.sizes), w.token_major("v", u, self.sizes))
+                        for u in self.units}
+        self.vel_host = {u: [w.velocity_input(u, s) for s in range(w.euler_steps)] for u in self.units}
+        self.eps_host = {u: w.eps(u) for u in self.units}
+        if host_only:
+            return
+        self.device = device
+        self.k = k.to(device)
+        self.v = v.to(device)
+        self.q = {u: t.to(device) for u, t in self.q_host.items()}
+        self.kv = {u: (a.to(device), b.to(device)) for u, (a, b) in self.kv_host.items()}
+        self.vel = {u: [t.to(device) for t in ts] for u, ts in self.vel_host.items()}
+        self.z = {u: self.eps_host[u].to(device) for u in self.units}
+        self.offs_dev = {u: torch.from_numpy(self.offsets_all[:u + 2].astype(np.int32)).to(device)
+                         for u in self.units}
+        q_max = max(self.sizes[u] for u in self.units)
+        self.out = torch.empty(q_max, H, D, dtype=torch.bfloat16, device=device)
+        from streaming_block_causal_flash_b300 import ws
+        need = max(ws.ws_block_causal_attn_workspace_size(self.sizes[u], int(self.offsets_all[u + 1]), H, D)
+                   for u in self.units)
+        self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        self.split = need > 0
+
+    def unit_flops(self, u: int) -> float:
+        offs = self.offsets_all[:u + 2]
+        rows = np.arange(int(offs[-2]), int(offs[-1]))
+        return attention_flops(offs, rows, self.w.heads, self.w.head_dim)
+
+    def launches_per_step(self) -> int:
+        return 1 + 1 + (1 if self.split else 0) + self.w.euler_steps
+
+
+def run_unit(sess: UnitSession, u: int, stream, ev=None):
+    """append -> attention -> Euler steps for unit u, all on `stream`."""
+    from streaming_block_causal_flash_b300 import ws
+    w = sess.w
+    n = sess.sizes[u]
+    offs = sess.offsets_all[:u + 2]
+    k_new, v_new = sess.kv[u]
+    if ev is not None:
+        ev[0].record(stream)
+    ws.ws_kv_append(k_new, v_new, sess.k, sess.v, int(offs[-2]), stream=stream)
+    if ev is not None:
+        ev[1].record(stream)
+    ws.ws_block_causal_attn(sess.q[u], sess.k, sess.v, sess.out[:n], offs, sess.offs_dev[u],
+                            workspace=sess.workspace, stream=stream)
+    if ev is not None:
+        ev[2].record(stream)
+    z = sess.z[u]
+    for s in range(w.euler_steps):
+        ws.ws_fm_euler_step(z, sess.vel[u][s], 1.0 / w.euler_steps, stream=stream)
+    if ev is not None:
+        ev[3].record(stream)
+
+
+# ------------------------------------------------------------- native arm
+
+def time_native(args, sess: UnitSession, device, world):
+    stream = torch.cuda.current_stream(device)
+    units = sess.units
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        run_unit(sess, units[i % len(units)], stream)
+    torch.cuda.synchronize(device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    flops = 0.0
+    for i in range(K):
+        u = units[i % len(units)]
+        run_unit(sess, u, stream, evs[i])
+        flops += sess.unit_flops(u)
+    stop.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    total_ms = start.elapsed_time(stop)
+    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    euler_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    return total_ms, flops, append_ms, attn_ms, euler_ms
+
+
+def time_e2e(args, sess: UnitSession, device):
+    """Same step through the public API with host buffers: pinned host inputs
+    copied in and results copied out inside the timed region, every step."""
+    from streaming_block_causal_flash_b300 import ws
+    stream = torch.cuda.current_stream(device)
+    w = sess.w
+    u = sess.units[0]
+    n = sess.sizes[u]
+    offs = sess.offsets_all[:u + 2]
+    pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
+    h_q, (h_k, h_v) = pin(sess.q_host[u]), tuple(pin(t) for t in sess.kv_host[u])
+    h_vel = [pin(t) for t in sess.vel_host[u]]
+    h_eps = pin(sess.eps_host[u])
+    h_out = torch.empty(n, w.heads, w.head_dim, dtype=torch.bfloat16).pin_memory()
+    h_z = torch.empty_like(h_eps).pin_memory()
+    d_q = torch.empty_like(sess.q[u])
+    d_k, d_v = torch.empty_like(sess.kv[u][0]), torch.empty_like(sess.kv[u][1])
+    d_vel = [torch.empty_like(t) for t in sess.vel[u]]
+    d_z = torch.empty_like(sess.z[u])
+    h2d = sum(t.numel() * t.element_size() for t in [h_q, h_k, h_v, h_eps, *h_vel])
+    d2h = h_out.numel() * h_out.element_size() + h_z.numel() * h_z.element_size()
+
+    def step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_z.copy_(h_eps, non_blocking=True)
+        for d, h in zip(d_vel, h_vel):
+            d.copy_(h, non_blocking=True)
+        ws.ws_kv_append(d_k, d_v, sess.k, sess.v, int(offs[-2]), stream=stream)
+        ws.ws_block_causal_attn(d_q, sess.k, sess.v, sess.out[:n], offs, sess.offs_dev[u],
+                                workspace=sess.workspace, stream=stream)
+        for s in range(w.euler_steps):
+            ws.ws_fm_euler_step(d_z, d_vel[s], 1.0 / w.euler_steps, stream=stream)
+        h_out.copy_(sess.out[:n], non_blocking=True)
+        h_z.copy_(d_z, non_blocking=True)
+
+    steps = max(10, min(args.steps, 100))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(sess.unit_flops(u) / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def time_hbm_kernels(sess: UnitSession, device, peaks):
+    """Append and Euler alone, rotating buffer sets larger than L2."""
+    from streaming_block_causal_flash_b300 import ws
+    stream = torch.cuda.current_stream(device)
+    w = sess.w
+    H, D = w.heads, w.head_dim
+    u = sess.units[0]
+    n = sess.sizes[u]
+    slice_bytes = n * H * D * 2
+    nsets = max(4, int(3 * L2_BYTES // (4 * slice_bytes)) + 1)
+    ks = [torch.randn(n, H, D, device=device).to(torch.bfloat16) for _ in range(nsets)]
+    vs = [torch.randn(n, H, D, device=device).to(torch.bfloat16) for _ in range(nsets)]
+    cap_sets = max(1, sess.cap // n - 1)
+    out = {}
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 4 * nsets
+    for i in range(nsets):
+        ws.ws_kv_append(ks[i], vs[i], sess.k, sess.v, (i % cap_sets) * n, stream=stream)
+    torch.cuda.synchronize(device)
+    a.record(stream)
+    for i in range(reps):
+        ws.ws_kv_append(ks[i % nsets], vs[i % nsets], sess.k, sess.v, (i % cap_sets) * n, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    us = a.elapsed_time(b) * 1e3 / reps
+    byts = 4.0 * slice_bytes
+    out["append"] = {"us": round(us, 2), "bytes": int(byts), "gbs": round(byts / us / 1e3, 1),
+                     "frac_hbm": round(byts / us / 1e3 / peaks["hbm_gbs"], 3)}
+    del ks, vs
+    nl = w.latent_tokens * w.latent_channels
+    per = nl * (4 + 2 + 4)
+    zsets = max(4, int(3 * L2_BYTES // per) + 1)
+    zs = [torch.randn(nl, device=device) for _ in range(zsets)]
+    vls = [torch.randn(nl, device=device).to(torch.bfloat16) for _ in range(zsets)]
+    for i in range(zsets):
+        ws.ws_fm_euler_step(zs[i], vls[i], 0.25, stream=stream)
+    torch.cuda.synchronize(device)
+    reps = 4 * zsets
+    a.record(stream)
+    for i in range(reps):
+        ws.ws_fm_euler_step(zs[i % zsets], vls[i % zsets], 0.25, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    us = a.elapsed_time(b) * 1e3 / reps
+    out["euler"] = {"us": round(us, 2), "bytes": int(per), "gbs": round(per / us / 1e3, 1),
+                    "frac_hbm": round(per / us / 1e3 / peaks["hbm_gbs"], 3)}
+    out["method"] = f"CUDA events over back-to-back launches rotating {nsets}/{zsets} buffer sets (> L2)"
+    return out
+
+
+# ------------------------------------------------------------ oracle arms
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_unit_sample(sess: UnitSession, u: int, n_rows: int, heads=None):
+    """Time the oracle on a row sample of unit u; returns (seconds, flops)."""
+    from oracle import block_causal as bc
+    w = sess.w
+    offs = sess.offsets_all[:u + 2]
+    lo, hi = int(offs[-2]), int(offs[-1])
+    idx = np.unique(np.linspace(0, hi - lo - 1, n_rows).astype(np.int64))
+    heads = list(range(w.heads)) if heads is None else heads
+    e = int(offs[-1])
+    key = (u, tuple(heads))
+    cache = getattr(sess, "_f32_cache", None)
+    if cache is None or cache[0] != key:
+        # host-side data preparation (not timed): bf16 -> fp32, with unit u appended
+        k = sess.k_host[heads, :e].float().numpy()
+        v = sess.v_host[heads, :e].float().numpy()
+        k_new, v_new = sess.kv_host[u]
+        k[:, lo:hi] = k_new[:, heads].transpose(0, 1).float().numpy()
+        v[:, lo:hi] = v_new[:, heads].transpose(0, 1).float().numpy()
+        sess._f32_cache = (key, k, v)
+    _, k, v = sess._f32_cache
+    q = sess.q_host[u][idx][:, heads].float().numpy()
+    t0 = time.perf_counter()
+    bc.attention_rows(q, lo + idx, k, v, offs)
+    dt = time.perf_counter() - t0
+    flops = attention_flops(offs, lo + idx, len(heads), w.head_dim)
+    return dt, flops, idx.size, len(heads)
+
+
+def oracle_step_rest(sess: UnitSession, u: int):
+    """Oracle Euler steps over the unit's full latents; returns seconds."""
+    from oracle import flow_matching as fm
+    z = sess.eps_host[u].numpy()
+    vel = [t.float().numpy() for t in sess.vel_host[u]]
+    t0 = time.perf_counter()
+    for s in range(sess.w.euler_steps):
+        z = fm.euler_step(z, vel[s], 1.0 / sess.w.euler_steps)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(sess: UnitSession):
+    u = sess.units[0]
+    n_rows = 64
+    dt, flops, rows, heads = oracle_unit_sample(sess, u, n_rows)
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle, block-causal attention of {rows} evenly spaced query rows x "
+                      f"{heads} heads of unit {u} against {int(sess.offsets_all[u + 1])} keys "
+                      f"({flops / 1e9:.1f} GFLOP in {dt:.2f} s)"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    sess = UnitSession(w, None, host_only=True)
+    u = sess.units[0]
+    offs = sess.offsets_all[:u + 2]
+    n = sess.sizes[u]
+    heads = list(range(min(8, w.heads)))
+    n_rows = 8
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt_attn, flops_s, rows, nh = oracle_unit_sample(sess, u, n_rows, heads)
+        dt_rest = oracle_step_rest(sess, u)
+        # extrapolate the attention sample to the whole unit (rows x heads)
+        unit_ms = (dt_attn * (n / rows) * (w.heads / nh) + dt_rest) * 1e3
+        if i >= args.warmup:
+            times.append(unit_ms)
+    ms = statistics.mean(times)
+    value = sess.unit_flops(u) / (ms * 1e-3) / 1e12
+    cores = blas_threads()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, sess, u),
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"per step: fp64 oracle attention of {n_rows} query rows x {len(heads)} heads "
+                                       f"(extrapolated to the unit's {n} rows x {w.heads} heads) + "
+                                       f"{w.euler_steps} full Euler steps"},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def workload_config(w: Workload, sess: UnitSession, u: int):
+    offs = sess.offsets_all[:u + 2]
+    return {"workload": w.name, "heads": w.heads, "head_dim": w.head_dim,
+            "q_len": int(offs[-1] - offs[-2]), "kv_len": int(offs[-1]),
+            "history_units": w.history_units, "new_units": w.new_units,
+            "euler_steps": w.euler_steps, "latent": [w.latent_tokens, w.latent_channels],
+            "cache_capacity_tokens": sess.cap,
+            "l2": "inputs larger than L2: every step reads the full K/V cache "
+                  f"({2 * w.heads * int(offs[-1]) * w.head_dim * 2 / 1e9:.2f} GB)"}
+
+
+# --------------------------------------------------------------------- main
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        init_dist(world, "gloo")
+        line = reference_arm(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the hot path has no CPU fallback)")
+    from streaming_block_causal_flash_b300 import build as ws_build
+    from streaming_block_causal_flash_b300 import ws
+    ws_build.build()
+    ws.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    peaks = load_peaks()
+    w = WORKLOADS[args.workload]
+    sess = UnitSession(w, device)
+    clocks = ClockSampler(local)
+    clocks.start()
+    total_ms, flops, append_ms, attn_ms, euler_ms = time_native(args, sess, device, world)
+    clk = clocks.stop()
+    code, info = ws.ws_get_device_error()
+    if code != 0:
+        raise SystemExit(f"device error word set during the timed region: {info:#x}")
+    K = args.steps
+    local_ms = total_ms / K
+    max_ms, total_flops = reduce_over_ranks(local_ms, flops, world, device)
+    value = total_flops / (max_ms * 1e-3 * K) / 1e12
+
+    # roofline of the dominant call (attention: main kernel + combine)
+    attn_avg_ms = statistics.mean(attn_ms)
+    u0 = sess.units[0]
+    per_launch = statistics.mean(sess.unit_flops(sess.units[i % len(sess.units)]) for i in range(K))
+    achieved = per_launch / (attn_avg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": recorded_traffic(),
+                "kernel": "attn_tc_bf16_kernel (+ attn_combine_kernel) = one ws_block_causal_attn call",
+                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
+                if peaks["source"] == "measured" else "fallback 1.8 PFLOP/s"}
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(max_ms, 4),
+            "us_per_unit": round(max_ms * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1)*0.5 bf16 Q/K/V, N(0,1) latents and velocities",
+            "config": workload_config(w, sess, u0), "roofline": roofline,
+            "gpu_launches": sess.launches_per_step() * K, "clocks": clk,
+            "kernels_ms_mean": {"kv_append": round(statistics.mean(append_ms), 4),
+                                "block_causal_attn": round(attn_avg_ms, 4),
+                                "fm_euler_steps": round(statistics.mean(euler_ms), 4)}}
+    if not args.no_e2e:
+        e2e = time_e2e(args, sess, device)
+        e_ms, e_flops = reduce_over_ranks(e2e["ms_per_step"], sess.unit_flops(sess.units[0]), world, device)
+        e2e["value"] = round(e_flops / (e_ms * 1e-3) / 1e12, 3)
+        e2e["ms_per_step"] = round(e_ms, 4)
+        line["e2e"] = e2e
+    if rank == 0:
+        if not args.no_hbm:
+            line["hbm_kernels"] = time_hbm_kernels(sess, device, peaks)
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(sess)
+        print(json.dumps(line), flush=True)
+    barrier(world, device)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

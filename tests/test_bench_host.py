@@ -1,0 +1,67 @@
+"""Host-side logic of bench.py: the FLOP count, the over-ranks reduction
+(world size 2 on gloo), argument defaults and the traffic bookkeeping."""
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+from oracle import block_causal as bc
+
+
+def test_attention_flops_counts_visible_pairs():
+    offsets = np.array([0, 3, 3, 8, 12])
+    mask = bc.visibility_mask(offsets)
+    rows = np.arange(12)
+    assert bench.attention_flops(offsets, rows, heads=3, head_dim=16) == 4 * 16 * 3 * mask.sum()
+    last = np.arange(8, 12)       # the newest unit sees every key
+    assert bench.attention_flops(offsets, last, 1, 128) == 4 * 128 * 4 * 12
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    ms, work = bench.reduce_over_ranks(1.0 + rank, 10.0 * (rank + 1), world)
+    q.put((rank, ms, work))
+    torch.distributed.destroy_process_group()
+
+
+def test_reduce_over_ranks_takes_max_time_and_total_work():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 1000)
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, ms, work in res:
+        assert ms == 2.0 and work == 30.0
+
+
+def test_default_arguments_are_the_unit_640x368_bench():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.workload == "unit_640x368" and a.impl == "native"
+
+
+def test_recorded_traffic_is_null_when_kernel_changed(tmp_path, monkeypatch):
+    f = tmp_path / "t.txt"
+    f.write_text("dram_bytes_per_launch: 123\nkernel_source_sha256_16: deadbeef\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic() is None
+    f.write_text(f"dram_bytes_per_launch: 123\nkernel_source_sha256_16: {bench.source_digest(bench.ATTN_SOURCE)}\n")
+    assert bench.recorded_traffic() == 123.0
+
+
+def test_clock_sampler_without_nvidia_smi(monkeypatch):
+    def boom(*a, **k):
+        raise OSError("no nvidia-smi")
+    monkeypatch.setattr(bench.subprocess, "Popen", boom)
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.stop()["samples"] == 0
