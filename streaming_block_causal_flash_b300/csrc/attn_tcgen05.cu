@@ -8,13 +8,15 @@
 // directions, every earlier block, no later block.
 //   O_i = sum_{j<e(i)} softmax_j(s q_i.k_j) v_j,   LSE_i = ln sum_j exp(s q_i.k_j)
 //
-// CTA layout (one CTA per SM, 320 threads):
+// CTA layout (one CTA per SM, 384 threads):
 //   warps 0-3  softmax for query tile 0 (thread = one query row)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q tiles once per work item, then K_j, V_j into a
 //              5-slot ring of 32 KB slots (128 rows x 128 cols, two 128-byte
 //              swizzled column halves)
 //   warp  9    TMEM owner and single-thread MMA issuer
+//   warps 10-11 idle (they complete the third warpgroup, which gives up
+//              registers to the softmax warpgroups)
 // TMEM (512 columns): tile t uses S_t = cols [256t, 256t+128) (fp32 logits,
 // overwritten in place by bf16 P in its first 64 columns) and
 // O_t = cols [256t+128, 256t+256) (fp32 output accumulator).
@@ -64,7 +66,14 @@ constexpr int HD = 128;                       // head dim
 constexpr int NSTAGE = 5;                     // K/V ring slots
 constexpr int TILE_BYTES = BM * HD * 2;       // 32 KB
 constexpr int HALF_BYTES = TILE_BYTES / 2;    // 128 rows x 64 cols (128-byte rows)
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;
+// Register split: the two softmax warpgroups grow to REGS_SOFTMAX per thread,
+// the producer/MMA warpgroup shrinks to REGS_OTHER.  The sum must fit in what
+// the block is launched with (NUM_THREADS x the kernel's register count); the
+// host checks that before every launch.
+constexpr int REGS_SOFTMAX = 200;
+constexpr int REGS_OTHER = 96;
+constexpr int REGS_NEEDED = 256 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr float LN2 = 0.69314718055994531f;
@@ -183,9 +192,10 @@ __device__ __forceinline__ void record_error(int where) {
     g_attn_error[1] = (static_cast<unsigned>(where) << 16) | (blockIdx.x & 0xFFFFu);
 }
 
-// Bounded wait on an mbarrier phase (slow path).  Returns false on time-out
-// or when another role has already aborted the CTA.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+// Bounded wait on an mbarrier phase (slow path, inlined: a call inside a
+// setmaxnreg region would pin its register budget).  Returns false on
+// time-out or when another role has already aborted the CTA.
+__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned long long timeout_ns, int where) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -259,7 +269,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
+  // Each role's code sits inside the branch that sets its register budget,
+  // so the compiler allocates every region against the right limit.
+  if (warp >= 8) {
+  setmaxnreg_dec<REGS_OTHER>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -427,7 +440,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       wait_bar(bar(BAR_DRAIN), 0u, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_MMA);
     }
     __syncwarp();
+  }
   } else {
+    setmaxnreg_inc<REGS_SOFTMAX>();
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -468,15 +483,16 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             for (int i = 0; i < 32; ++i)
               if (kv0 + 32 * c + i >= e_row) s[c][i] = __float_as_uint(-INFINITY);
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        float mxc[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          mx0 = fmaxf(mx0, __uint_as_float(s[0][i]));
-          mx1 = fmaxf(mx1, __uint_as_float(s[1][i]));
-          mx2 = fmaxf(mx2, __uint_as_float(s[2][i]));
-          mx3 = fmaxf(mx3, __uint_as_float(s[3][i]));
+        for (int c = 0; c < 4; ++c) {
+          float a = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            a = max3f(a, __uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1]));
+          mxc[c] = a;
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * P.scale_log2;
+        const float m_tile = max3f(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3])) * P.scale_log2;
         const bool need = m_tile > m + RESCALE_LOG2;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? m_tile : m;
@@ -496,19 +512,24 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           m = m_new;
         }
         const float mb = (m == -INFINITY) ? 0.f : m;
-        const float sc = P.scale_log2;
-        float l0 = 0.f, l1 = 0.f;
-        // p = 2^(x - m); packed in place: bf16 pair k of chunk c overwrites
-        // s[c][k] (both sources s[c][2k], s[c][2k+1] are already consumed),
-        // then columns 16c..16c+15 of S_t receive P[32c .. 32c+31].
+        // p = 2^(x*scale - m), pairs in packed fp32x2 arithmetic; the bf16
+        // pair k of chunk c overwrites s[c][k] (both of its sources are
+        // already consumed), then columns 16c..16c+15 of S_t receive
+        // P[32c .. 32c+31].
+        const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
+        const uint64_t nm2 = f2_pack(-mb, -mb);
+        uint64_t lsum[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * k]), sc, -mb));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * k + 1]), sc, -mb));
-            l0 += p0;
-            l1 += p1;
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[c][2 * k]),
+                                               __uint_as_float(s[c][2 * k + 1])), sc2, nm2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            lsum[k & 1] = f2_add(lsum[k & 1], f2_pack(p0, p1));
             s[c][k] = pack_bf16x2(p0, p1);
           }
           uint32_t pk[16];
@@ -516,7 +537,12 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           for (int k = 0; k < 16; ++k) pk[k] = s[c][k];
           tmem_st16(tS + 16u * c, pk);
         }
-        l += l0 + l1;
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(lsum[0], a0, a1);
+          f2_unpack(lsum[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(BAR_P_FULL + t));
@@ -695,6 +721,12 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
     err = cudaFuncSetAttribute(attn_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SMEM_ALLOC);
     if (err != cudaSuccess) return err;
+    // The warpgroup register split must fit in the registers the block is
+    // launched with, or setmaxnreg.inc would wait forever: refuse instead.
+    cudaFuncAttributes fa{};
+    err = cudaFuncGetAttributes(&fa, attn_tc_bf16_kernel);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
     attr_done[dev] = true;
   }
   Params P{};

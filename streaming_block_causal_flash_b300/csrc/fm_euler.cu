@@ -33,6 +33,45 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+template <bool kVBf16>
+__device__ __forceinline__ void load_v8(const void* v_raw, int64_t i, float (&vf)[8]) {
+  if constexpr (kVBf16) {
+    const uint4 vv = reinterpret_cast<const uint4*>(v_raw)[i];
+    bf16x8_to_f32(vv, vf);
+  } else {
+    const float4 a = ld_f4(static_cast<const float*>(v_raw) + 8 * i);
+    const float4 b = ld_f4(static_cast<const float*>(v_raw) + 8 * i + 4);
+    vf[0] = a.x; vf[1] = a.y; vf[2] = a.z; vf[3] = a.w;
+    vf[4] = b.x; vf[5] = b.y; vf[6] = b.z; vf[7] = b.w;
+  }
+}
+
+template <bool kOutBf16>
+__device__ __forceinline__ void update8(float* __restrict__ z, __nv_bfloat16* __restrict__ zb,
+                                        int64_t i, float4 z0, float4 z1, const float (&vf)[8],
+                                        float neg) {
+  z0.x = fmaf(neg, vf[0], z0.x);
+  z0.y = fmaf(neg, vf[1], z0.y);
+  z0.z = fmaf(neg, vf[2], z0.z);
+  z0.w = fmaf(neg, vf[3], z0.w);
+  z1.x = fmaf(neg, vf[4], z1.x);
+  z1.y = fmaf(neg, vf[5], z1.y);
+  z1.z = fmaf(neg, vf[6], z1.z);
+  z1.w = fmaf(neg, vf[7], z1.w);
+  reinterpret_cast<float4*>(z)[2 * i] = z0;
+  reinterpret_cast<float4*>(z)[2 * i + 1] = z1;
+  if constexpr (kOutBf16) {
+    uint4 o;
+    o.x = f32x2_to_bf16x2(z0.x, z0.y);
+    o.y = f32x2_to_bf16x2(z0.z, z0.w);
+    o.z = f32x2_to_bf16x2(z1.x, z1.y);
+    o.w = f32x2_to_bf16x2(z1.z, z1.w);
+    reinterpret_cast<uint4*>(zb)[i] = o;
+  }
+}
+
+// Each thread step handles two groups of eight elements, one grid stride
+// apart, with all loads issued before the stores.
 template <bool kVBf16, bool kOutBf16>
 __global__ void __launch_bounds__(kThreads)
 fm_euler_kernel(float* __restrict__ z, const void* __restrict__ v_raw,
@@ -40,37 +79,22 @@ fm_euler_kernel(float* __restrict__ z, const void* __restrict__ v_raw,
   const int64_t n8 = n / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   const float neg = -dtau;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n8; i += stride) {
-    float4 z0 = ld_f4(z + 8 * i);
-    float4 z1 = ld_f4(z + 8 * i + 4);
-    float vf[8];
-    if constexpr (kVBf16) {
-      const uint4 vv = reinterpret_cast<const uint4*>(v_raw)[i];
-      bf16x8_to_f32(vv, vf);
-    } else {
-      const float4 a = ld_f4(static_cast<const float*>(v_raw) + 8 * i);
-      const float4 b = ld_f4(static_cast<const float*>(v_raw) + 8 * i + 4);
-      vf[0] = a.x; vf[1] = a.y; vf[2] = a.z; vf[3] = a.w;
-      vf[4] = b.x; vf[5] = b.y; vf[6] = b.z; vf[7] = b.w;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n8;
+       i += 2 * stride) {
+    const int64_t j = i + stride;
+    const bool has_j = j < n8;
+    const float4 a0 = ld_f4(z + 8 * i);
+    const float4 a1 = ld_f4(z + 8 * i + 4);
+    float va[8], vb[8];
+    load_v8<kVBf16>(v_raw, i, va);
+    float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+    if (has_j) {
+      b0 = ld_f4(z + 8 * j);
+      b1 = ld_f4(z + 8 * j + 4);
+      load_v8<kVBf16>(v_raw, j, vb);
     }
-    z0.x = fmaf(neg, vf[0], z0.x);
-    z0.y = fmaf(neg, vf[1], z0.y);
-    z0.z = fmaf(neg, vf[2], z0.z);
-    z0.w = fmaf(neg, vf[3], z0.w);
-    z1.x = fmaf(neg, vf[4], z1.x);
-    z1.y = fmaf(neg, vf[5], z1.y);
-    z1.z = fmaf(neg, vf[6], z1.z);
-    z1.w = fmaf(neg, vf[7], z1.w);
-    reinterpret_cast<float4*>(z)[2 * i] = z0;
-    reinterpret_cast<float4*>(z)[2 * i + 1] = z1;
-    if constexpr (kOutBf16) {
-      uint4 o;
-      o.x = f32x2_to_bf16x2(z0.x, z0.y);
-      o.y = f32x2_to_bf16x2(z0.z, z0.w);
-      o.z = f32x2_to_bf16x2(z1.x, z1.y);
-      o.w = f32x2_to_bf16x2(z1.z, z1.w);
-      reinterpret_cast<uint4*>(zb)[i] = o;
-    }
+    update8<kOutBf16>(z, zb, i, a0, a1, va, neg);
+    if (has_j) update8<kOutBf16>(z, zb, j, b0, b1, vb, neg);
   }
   // ragged tail (n not a multiple of 8): the first block finishes it
   if (blockIdx.x == 0) {
@@ -93,7 +117,7 @@ cudaError_t launch_fm_euler(float* z, const void* v, bool v_is_bf16, void* z_bf1
                             int64_t n, float dtau, int num_sms, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int64_t n8 = n / 8;
-  int64_t blocks = (n8 + kThreads - 1) / kThreads;
+  int64_t blocks = (n8 + 2 * kThreads - 1) / (2 * kThreads);
   const int64_t cap_blocks = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap_blocks) blocks = cap_blocks;
   if (blocks < 1) blocks = 1;

@@ -4,15 +4,15 @@
 // cache ("全双工语音模型精读⑫：Wan-Streamer" (alwayszhang.cn), 四、推理, step 3).
 // Slice layout [n][H][row] (token-major, as a projection emits it); cache
 // layout [H][capacity][row].  Pure data movement: every thread moves 16-byte
-// chunks, K and V in one launch, several independent loads in flight before
-// the matching stores.
+// chunks, K and V in one launch (grid.y), several independent loads in
+// flight before the matching stores.
 #include "ws_internal.h"
 
 namespace ws {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kThreads = 128;
+constexpr int kMaxPerThread = 8;   // 16-byte chunks per thread held in flight
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -22,38 +22,35 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
-// Chunk index c runs over [2][n][H][CH]: tensor (K, V), token, head, 16-byte
-// column.  Reads are contiguous in c; each cache row of CH chunks is written
-// contiguously.
+// One block per (tensor, token): it moves that token's [H][row] slice
+// (heads * CH 16-byte chunks, contiguous in the source) into row
+// cache_len + token of every head.  Chunk c of the slice belongs to head
+// c / CH, column c % CH.  All loads of a thread are issued before its stores.
 __global__ void __launch_bounds__(kThreads)
 kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                  uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int64_t cache_len,
-                 int64_t n_new, int64_t capacity, int heads, int CH) {
-  const int64_t per_tensor = n_new * heads * CH;
-  const int64_t total = 2 * per_tensor;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; base < total;
-       base += stride * kUnroll) {
-    uint4 val[kUnroll];
-    uint4* dst[kUnroll];
+                 int64_t capacity, int heads, int CH) {
+  const int64_t t = blockIdx.x;
+  const bool is_v = blockIdx.y != 0;
+  const int per_token = heads * CH;
+  const uint4* src = (is_v ? v_new : k_new) + t * per_token;
+  uint4* dst = (is_v ? v_cache : k_cache) + (cache_len + t) * CH;
+  const int64_t head_stride = capacity * CH;
+  for (int base = threadIdx.x; base < per_token; base += kThreads * kMaxPerThread) {
+    uint4 val[kMaxPerThread];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + u * stride;
-      dst[u] = nullptr;
-      if (c < total) {
-        const bool is_v = c >= per_tensor;
-        const int64_t i = is_v ? c - per_tensor : c;
-        const int64_t col = i % CH;
-        const int64_t th = i / CH;
-        const int64_t h = th % heads;
-        const int64_t t = th / heads;
-        val[u] = ld_stream((is_v ? v_new : k_new) + i);
-        dst[u] = (is_v ? v_cache : k_cache) + ((h * capacity + cache_len + t) * CH + col);
-      }
+    for (int u = 0; u < kMaxPerThread; ++u) {
+      const int c = base + u * kThreads;
+      if (c < per_token) val[u] = ld_stream(src + c);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (dst[u]) *dst[u] = val[u];
+    for (int u = 0; u < kMaxPerThread; ++u) {
+      const int c = base + u * kThreads;
+      if (c < per_token) {
+        const int h = c / CH;
+        dst[h * head_stride + (c - h * CH)] = val[u];
+      }
+    }
   }
 }
 
@@ -62,17 +59,14 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              int64_t cache_len, int64_t n_new, int64_t capacity, int heads,
                              int row_bytes, int num_sms, cudaStream_t s) {
+  (void)num_sms;
   const int CH = row_bytes / 16;
-  const int64_t total = 2 * n_new * heads * CH;
-  if (total == 0) return cudaSuccess;
-  const int64_t per_block = static_cast<int64_t>(kThreads) * kUnroll;
-  int64_t blocks = (total + per_block - 1) / per_block;
-  const int64_t cap_blocks = static_cast<int64_t>(num_sms) * 8;   // 8 x 256 threads per SM
-  if (blocks > cap_blocks) blocks = cap_blocks;
-  kv_append_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+  if (n_new == 0) return cudaSuccess;
+  if (n_new > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(n_new), 2);
+  kv_append_kernel<<<grid, kThreads, 0, s>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), cache_len, n_new, capacity,
-      heads, CH);
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), cache_len, capacity, heads, CH);
   return cudaGetLastError();
 }
 

@@ -242,6 +242,8 @@ ws_status ws_kv_append(const void* k_new, const void* v_new, void* k_cache, void
   const int64_t row_bytes = (int64_t)head_dim * (int64_t)dtype_size(dt);
   if (row_bytes % 16 != 0)
     return fail(WS_ERR_UNSUPPORTED, "%s: head_dim*sizeof(dtype) must be a multiple of 16", who);
+  if ((int64_t)num_heads * row_bytes > (int64_t)INT32_MAX || n_new > (int64_t)INT32_MAX)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: slice too large", who);
   if (n_new == 0) return ok();
   if (!k_new || !v_new || !k_cache || !v_cache)
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer argument", who);
