@@ -151,6 +151,48 @@ WS_API ws_status ws_fm_euler_step(void* z, ws_dtype z_dt, const void* v, ws_dtyp
                            ws_stream_t stream);
 
 /*
+ * ws_block_causal_attn_noalloc -- ws_block_causal_attn for callers that
+ * cannot allocate device memory.  The paper has no counterpart: this is a
+ * deployment convenience of this library.
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocating library
+ * routine -- a plug-in inside a host process whose memory pool it does not
+ * own, or a real-time loop where an allocator call (which can block and
+ * synchronise the device) is not allowed.  Such a caller cannot provide the
+ * split-KV workspace that ws_block_causal_attn takes.
+ *
+ * What it does: exactly what ws_block_causal_attn does (same arguments
+ * without workspace/workspace_bytes, same kernels, same results), with the
+ * workspace taken from one static device array of WS_NOALLOC_SCRATCH_BYTES
+ * (40 MiB) built into the library.  The driver reserves that array on every
+ * GPU that loads the library, and keeps it until the process exits.  The call
+ * itself allocates nothing.
+ *
+ * Limits and rules:
+ *  - Sizes whose workspace (ws_block_causal_attn_workspace_size) exceeds
+ *    WS_NOALLOC_SCRATCH_BYTES are rejected with WS_ERR_CAPACITY and a message
+ *    saying so; nothing is launched.  40 MiB covers every unit call on a GPU
+ *    of up to 158 SMs (a B300 has 148).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call before any stream capture on the device.
+ *  - All calls on a device share the one array.  Its contents on entry do not
+ *    matter (every value read is written earlier in the same call), but two
+ *    calls that may overlap on the GPU -- on different streams, or from
+ *    different threads -- race on it and corrupt each other's results.
+ *    Serialise them (one stream, or events between them).
+ * Errors: as ws_block_causal_attn, plus WS_ERR_CAPACITY for the limit above
+ * and WS_ERR_CUDA if the array's address cannot be looked up.
+ */
+#define WS_NOALLOC_SCRATCH_BYTES ((size_t)40 * 1024 * 1024)
+WS_API ws_status ws_block_causal_attn_noalloc(const void* q, const void* k_cache,
+                                              const void* v_cache, void* out, float* lse_or_null,
+                                              const int32_t* h_offsets, const int32_t* d_offsets,
+                                              int n_blocks, int64_t capacity, int num_heads,
+                                              int head_dim, float softmax_scale, ws_dtype dt,
+                                              ws_stream_t stream);
+
+/*
  * Bytes of workspace ws_block_causal_attn needs for these sizes on the
  * current device (0 when no key range is split).  Returns SIZE_MAX when the
  * sizes are invalid or the device cannot be queried.

@@ -205,6 +205,14 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
 
 }  // namespace
 
+namespace ws {
+
+// Lets entry points defined in other files report a failure through
+// ws_last_error() on the calling thread.
+ws_status record_failure(ws_status s, const char* msg) { return fail(s, "%s", msg); }
+
+}  // namespace ws
+
 extern "C" {
 
 int ws_abi_version(void) { return 100; }

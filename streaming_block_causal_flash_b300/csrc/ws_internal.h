@@ -5,7 +5,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/ws.h"
+
 namespace ws {
+
+// Sets the thread-local ws_last_error() message and returns s (ws_api.cu).
+ws_status record_failure(ws_status s, const char* msg);
 
 // ---- KV append (kv_append.cu)
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
