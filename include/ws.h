@@ -221,6 +221,17 @@ WS_API ws_status ws_clear_device_error(void);
  */
 WS_API ws_status ws_set_wait_timeout_ns(uint64_t timeout_ns);
 
+/*
+ * Test hook for failure detection, off by default, process wide.  While on,
+ * every tensor-core attention launch makes one of its MMA issuers wait on a
+ * barrier that nothing completes.  The wait limit (ws_set_wait_timeout_ns)
+ * runs out, the kernel records the wait site in the device error word, every
+ * role stops, drains its own copies and MMAs, frees its tensor memory and
+ * returns; ws_get_device_error() then reports WS_ERR_TIMEOUT.  Outputs of
+ * such a launch are undefined.  Nothing faults, traps or hangs.
+ */
+WS_API ws_status ws_debug_force_wait_timeout(int on);
+
 /* ABI version of this header (major * 100 + minor). */
 WS_API int ws_abi_version(void);
 

@@ -14,19 +14,23 @@
 //   warp  8    TMA producer: Q tiles once per work item, then K_j, V_j into a
 //              5-slot ring of 32 KB slots (128 rows x 128 cols, two 128-byte
 //              swizzled column halves)
-//   warp  9    TMEM owner and single-thread MMA issuer
-//   warps 10-11 idle (they complete the third warpgroup, which gives up
+//   warp  9    TMEM owner; its lane 0 issues every MMA of query tile 0
+//   warp  10   lane 0 issues every MMA of query tile 1 (two issuers keep the
+//              tensor pipe fed while the other one waits on barriers)
+//   warp  11   idle (it completes the third warpgroup, which gives up
 //              registers to the softmax warpgroups)
 // TMEM (512 columns): tile t uses S_t = cols [256t, 256t+128) (fp32 logits,
 // overwritten in place by bf16 P in its first 64 columns) and
 // O_t = cols [256t+128, 256t+256) (fp32 output accumulator).
 //
-// Per key tile j, the MMA thread issues, in this order,
-//   PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j)
-// so that while one softmax group works on S_t(j) the tensor pipe has the
-// other tile's PV and QK queued.  tcgen05.mma instructions from one thread
-// execute in issue order, which orders QK_t(j) (writes S_t) after PV_t(j-1)
-// (reads P_t from the same columns).
+// Per key tile j, the issuer of query tile t issues PV_t(j-1) then QK_t(j);
+// the two issuers run independently, so while one softmax group works on
+// S_t(j) the tensor pipe executes the other tile's PV and QK.  tcgen05.mma
+// instructions from one thread execute in issue order, which orders QK_t(j)
+// (writes S_t) after PV_t(j-1) (reads P_t from the same columns).  One
+// thread issuing both tiles' MMAs left the pipe idle during its barrier
+// waits and fences (about 115 cycles per 64-cycle MMA); two issuers hide
+// that bookkeeping behind each other's MMAs.
 //
 // Softmax keeps a per-row running max m (log2 units of the scaled logits) and
 // sum l.  O is rescaled only when a row's max grows by more than 2^8 (lazy
@@ -89,19 +93,20 @@ constexpr int BAR_S_FULL = BAR_Q_EMPTY + 1;   // [2]
 constexpr int BAR_P_FULL = BAR_S_FULL + 2;    // [2]
 constexpr int BAR_O_FULL = BAR_P_FULL + 2;    // [2]
 constexpr int BAR_O_FREE = BAR_O_FULL + 2;    // [2]
-constexpr int BAR_DRAIN = BAR_O_FREE + 2;
-constexpr int NUM_BARS = BAR_DRAIN + 1;
+constexpr int BAR_DRAIN = BAR_O_FREE + 2;    // [2], one per MMA issuer
+constexpr int BAR_STALL = BAR_DRAIN + 2;      // never completed (test hook)
+constexpr int NUM_BARS = BAR_STALL + 1;
 
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = 2 * TILE_BYTES;
 constexpr int SMEM_BARS = SMEM_KV + NSTAGE * TILE_BYTES;
 constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_MISC + 16;
+constexpr int SMEM_USED = SMEM_MISC + 16;   // tmem slot, abort flag, issue lock
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 // wait sites (error info)
 enum : int { W_PROD_QE = 1, W_PROD_KVE, W_MMA_Q, W_MMA_KV, W_MMA_P, W_MMA_OF, W_SM_S, W_SM_O,
-             W_DRAIN_MMA, W_DRAIN_TMA };
+             W_DRAIN_MMA, W_DRAIN_TMA, W_FORCED, W_LOCK };
 
 struct Params {
   int prefill;
@@ -116,6 +121,7 @@ struct Params {
   float* ws_o;     // [grid*2][256][HD]
   float* ws_lse;   // [grid*2][256]
   unsigned long long timeout_ns;
+  int force_stall;   // test hook: one MMA issuer waits on a barrier nothing completes
 };
 
 struct Item {
@@ -217,6 +223,29 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return wait_bar_slow(bar, parity, abort_flag, timeout_ns, where);
 }
 
+// Issue lock shared by the two MMA issuers: a tile's PV and QK go to the
+// tensor pipe as one uninterrupted group (interleaving the two tiles' groups
+// delays both tiles' logits).  The holder only issues and commits, which
+// never blocks indefinitely; waiting for the lock is bounded like every wait.
+__device__ __forceinline__ bool issue_lock(int* lk, volatile int* abort_flag,
+                                           unsigned long long timeout_ns) {
+  if (atomicCAS(lk, 0, 1) == 0) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (atomicCAS(lk, 0, 1) == 0) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        record_error(W_LOCK);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void issue_unlock(int* lk) { atomicExch(lk, 0); }
+
 struct Ring {
   uint32_t stage = 0, phase = 0;
   __device__ __forceinline__ void advance() {
@@ -239,6 +268,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t sBar = sbase + SMEM_BARS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + SMEM_MISC + 4);
+  int* issue_lk = reinterpret_cast<int*>(sgen + SMEM_MISC + 8);
   auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x >> 5;
@@ -247,10 +277,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), 1);
-      mbar_init(bar(BAR_KV_EMPTY + s), 1);
+      mbar_init(bar(BAR_KV_EMPTY + s), 2);      // released by both MMA issuers
     }
     mbar_init(bar(BAR_Q_FULL), 1);
-    mbar_init(bar(BAR_Q_EMPTY), 1);
+    mbar_init(bar(BAR_Q_EMPTY), 2);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(BAR_S_FULL + t), 1);
       mbar_init(bar(BAR_P_FULL + t), 128);
@@ -258,7 +288,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(bar(BAR_O_FREE + t), 128);
     }
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_DRAIN + 1), 1);
+    mbar_init(bar(BAR_STALL), 1);
     *abort_flag = 0;
+    *issue_lk = 0;
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -335,109 +368,115 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                  DRAIN_TIMEOUT_NS, W_DRAIN_TMA);
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------- MMA issuers, one per query tile
+    // Two issuing threads keep the tensor pipe fed: while one waits on its
+    // barriers and fences, the other's MMAs execute.  Each issuer walks the
+    // same K/V ring and, for every slot use, waits for the slot to be full
+    // before it commits its release, so a slot's two releases (count-2
+    // barrier) always belong to the same fill.
     if (lane == 0) {
+      const int t = warp - 9;
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, 0, 1);
+      const uint32_t aQ = sQ + t * TILE_BYTES;
+      const uint32_t tS = tmem + 256u * t;
+      const uint32_t tO = tS + 128u;
       ItemIter it;
       iter_init(P, it);
       Item item;
       Ring ring;
-      uint32_t q_phase = 0;
-      uint32_t p_phase[2] = {0u, 0u};
-      uint32_t of_phase[2] = {0u, 0u};
+      uint32_t q_phase = 0, p_phase = 0, of_phase = 0;
       bool ok = true;
 
-      auto issue_qk = [&](int t, uint32_t kslot) {
-        const uint32_t a0 = sQ + t * TILE_BYTES;
+      auto issue_qk = [&](uint32_t kslot) {
         const uint32_t b0 = sKV + kslot * TILE_BYTES;
-        const uint32_t d = tmem + 256u * t;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-          mma_ss(d, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024),
+          mma_ss(tS, smem_desc_sw128(aQ + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024),
                  IDESC_QK, k > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+      auto issue_pv = [&](uint32_t vslot, bool acc) {
         const uint32_t b0 = sKV + vslot * TILE_BYTES;
-        const uint32_t d = tmem + 256u * t + 128u;
-        const uint32_t a = tmem + 256u * t;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          mma_ts(d, a + 8u * k, smem_desc_sw128(b0 + k * 16 * 128, HALF_BYTES, 1024), IDESC_PV,
+          mma_ts(tO, tS + 8u * k, smem_desc_sw128(b0 + k * 16 * 128, HALF_BYTES, 1024), IDESC_PV,
                  (acc || k > 0) ? 1u : 0u);
         }
       };
 
+      if (P.force_stall && t == 0) {
+        // Test hook: wait on a barrier that nothing completes, so the wait
+        // limit runs out and every role takes the give-up path.
+        wait_bar(bar(BAR_STALL), 0u, abort_flag, P.timeout_ns, W_FORCED);
+        ok = false;
+      }
       while (ok && iter_next(P, it, item)) {
         const int n_iter = max(item.n[0], item.n[1]);
+        const int n = item.n[t];
         if (!wait_bar(bar(BAR_Q_FULL), q_phase, abort_flag, P.timeout_ns, W_MMA_Q)) break;
         q_phase ^= 1u;
-        tc_fence_after();
         // prologue: QK_t(0)
         const uint32_t k0 = ring.stage;
         if (!wait_bar(bar(BAR_KV_FULL + ring.stage), ring.phase, abort_flag, P.timeout_ns,
                       W_MMA_KV)) break;
         ring.advance();
         tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (item.n[t] > 0) {
-            issue_qk(t, k0);
-            mma_commit(bar(BAR_S_FULL + t));
-          }
+        if (n > 0) {
+          if (!issue_lock(issue_lk, abort_flag, P.timeout_ns)) break;
+          issue_qk(k0);
+          mma_commit(bar(BAR_S_FULL + t));
+          issue_unlock(issue_lk);
         }
         mma_commit(bar(BAR_KV_EMPTY + k0));
-        if (n_iter == 1) mma_commit(bar(BAR_Q_EMPTY));
+        if (n <= 1) mma_commit(bar(BAR_Q_EMPTY));
 
-        for (int jj = 0; jj < n_iter && ok; ++jj) {
+        for (int jj = 0; jj < n_iter; ++jj) {
           const uint32_t vslot = ring.stage;
           if (!wait_bar(bar(BAR_KV_FULL + ring.stage), ring.phase, abort_flag, P.timeout_ns,
                         W_MMA_KV)) { ok = false; break; }
           ring.advance();
-          tc_fence_after();
           const bool more = jj + 1 < n_iter;
           uint32_t kslot = 0, kphase = 0;
           if (more) { kslot = ring.stage; kphase = ring.phase; ring.advance(); }
-          bool k_ready = false;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (jj >= item.n[t]) continue;
-            if (!wait_bar(bar(BAR_P_FULL + t), p_phase[t], abort_flag, P.timeout_ns, W_MMA_P)) {
+          // every wait and fence of this step before taking the issue lock
+          if (jj < n) {
+            if (!wait_bar(bar(BAR_P_FULL + t), p_phase, abort_flag, P.timeout_ns, W_MMA_P)) {
               ok = false; break;
             }
-            p_phase[t] ^= 1u;
+            p_phase ^= 1u;
             if (jj == 0) {
-              if (!wait_bar(bar(BAR_O_FREE + t), of_phase[t] ^ 1u, abort_flag, P.timeout_ns,
+              if (!wait_bar(bar(BAR_O_FREE + t), of_phase ^ 1u, abort_flag, P.timeout_ns,
                             W_MMA_OF)) { ok = false; break; }
-              of_phase[t] ^= 1u;
+              of_phase ^= 1u;
             }
+          }
+          if (more && !wait_bar(bar(BAR_KV_FULL + kslot), kphase, abort_flag, P.timeout_ns,
+                                W_MMA_KV)) { ok = false; break; }
+          if (jj < n) {
             tc_fence_after();
-            issue_pv(t, vslot, jj > 0);
-            if (jj + 1 < item.n[t]) {
-              if (!k_ready) {
-                if (!wait_bar(bar(BAR_KV_FULL + kslot), kphase, abort_flag, P.timeout_ns,
-                              W_MMA_KV)) { ok = false; break; }
-                tc_fence_after();
-                k_ready = true;
-              }
-              issue_qk(t, kslot);
+            if (!issue_lock(issue_lk, abort_flag, P.timeout_ns)) { ok = false; break; }
+            issue_pv(vslot, jj > 0);
+            if (jj + 1 < n) {
+              issue_qk(kslot);
               mma_commit(bar(BAR_S_FULL + t));
             } else {
               mma_commit(bar(BAR_O_FULL + t));
             }
+            issue_unlock(issue_lk);
           }
-          if (!ok) break;
           mma_commit(bar(BAR_KV_EMPTY + vslot));
           if (more) mma_commit(bar(BAR_KV_EMPTY + kslot));
-          if (jj + 2 == n_iter) mma_commit(bar(BAR_Q_EMPTY));
+          if (jj + 2 == n) mma_commit(bar(BAR_Q_EMPTY));
         }
       }
       // Teardown: all MMAs this thread issued must be complete before the
       // tensor memory is released.
-      mma_commit(bar(BAR_DRAIN));
+      mma_commit(bar(BAR_DRAIN + t));
       volatile int no_abort = 0;
-      wait_bar(bar(BAR_DRAIN), 0u, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_MMA);
+      wait_bar(bar(BAR_DRAIN + t), 0u, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_MMA);
     }
     __syncwarp();
   }
@@ -750,6 +789,7 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
     P.ws_lse = P.ws_o + static_cast<size_t>(plan.grid) * 2 * 256 * HD;
   }
   P.timeout_ns = timeout_ns;
+  P.force_stall = a.force_stall;
   attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, P);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

@@ -17,6 +17,7 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 uint64_t g_timeout_ns = 2000000000ull;
+int g_force_stall = 0;
 
 ws_status fail(ws_status s, const char* fmt, ...) {
   va_list ap;
@@ -198,6 +199,7 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   a.capacity = capacity;
   a.scale = scale;
   a.workspace = workspace;
+  a.force_stall = g_force_stall;
   cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, g_timeout_ns, stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
@@ -234,6 +236,11 @@ const char* ws_last_error(void) { return g_last_error; }
 ws_status ws_set_wait_timeout_ns(uint64_t timeout_ns) {
   if (timeout_ns == 0) return fail(WS_ERR_INVALID_ARGUMENT, "ws_set_wait_timeout_ns: must be > 0");
   g_timeout_ns = timeout_ns;
+  return ok();
+}
+
+ws_status ws_debug_force_wait_timeout(int on) {
+  g_force_stall = on ? 1 : 0;
   return ok();
 }
 

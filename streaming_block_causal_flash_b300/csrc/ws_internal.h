@@ -73,6 +73,7 @@ struct TcAttnArgs {
   int64_t capacity;
   float scale;           // softmax scale (natural units)
   void* workspace;
+  int force_stall;       // test hook (ws_debug_force_wait_timeout)
 };
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,

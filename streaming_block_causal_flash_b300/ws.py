@@ -48,6 +48,7 @@ SIGNATURES = {
     "ws_get_device_error": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "ws_clear_device_error": (_c_int, []),
     "ws_set_wait_timeout_ns": (_c_int, [_c_u64]),
+    "ws_debug_force_wait_timeout": (_c_int, [_c_int]),
     "ws_abi_version": (_c_int, []),
 }
 
@@ -234,6 +235,11 @@ def ws_clear_device_error() -> None:
 
 def ws_set_wait_timeout_ns(ns: int) -> None:
     _check(load().ws_set_wait_timeout_ns(int(ns)))
+
+
+def ws_debug_force_wait_timeout(on: bool) -> None:
+    """Test hook: make tensor-core attention launches give up on a wait."""
+    _check(load().ws_debug_force_wait_timeout(1 if on else 0))
 
 
 def ws_abi_version() -> int:
