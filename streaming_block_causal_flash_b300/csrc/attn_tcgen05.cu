@@ -34,8 +34,11 @@
 //
 // Softmax keeps a per-row running max m (log2 units of the scaled logits) and
 // sum l.  O is rescaled only when a row's max grows by more than 2^8 (lazy
-// rescale; exact after the final division by l).  P is rounded to bf16 before
-// PV.
+// rescale; exact after the final division by l).  After a row's first tile
+// the exponentials are computed against the current m with no tile max at
+// all; only a tile whose row sum exceeds 2^64 is redone exactly (tile max,
+// rescale) from S, which stays in TMEM until P is stored.  P is rounded to
+// bf16 before PV.
 //
 // Work decomposition:
 //  * unit mode (the query block is the newest unit; every row sees all keys
@@ -80,6 +83,9 @@ constexpr int REGS_OTHER = 96;
 constexpr int REGS_NEEDED = 256 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
+// A tile computed against a row max it has outgrown is accepted while the
+// row's sum of p stays within this bound (so every p does).
+constexpr float SPEC_SUM_LIMIT = 18446744073709551616.0f;   // 2^64
 constexpr float LN2 = 0.69314718055994531f;
 // Teardown waits (copies / MMAs still in flight) never use a shorter limit.
 constexpr unsigned long long DRAIN_TIMEOUT_NS = 2000000000ull;
@@ -245,6 +251,56 @@ __device__ __forceinline__ bool issue_lock(int* lk, volatile int* abort_flag,
 }
 
 __device__ __forceinline__ void issue_unlock(int* lk) { atomicExch(lk, 0); }
+
+// Keys at or beyond the row's limit get -inf logits (ragged key tail and,
+// in prefill mode, keys of later blocks).
+__device__ __forceinline__ void mask_tail(uint32_t (&s)[4][32], int kv0, int e_row) {
+  if (kv0 + BN > e_row) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (kv0 + 32 * c + i >= e_row) s[c][i] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Row max of the 128 raw logits held by this thread.
+__device__ __forceinline__ float tile_max(const uint32_t (&s)[4][32]) {
+  float mxc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float a = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      a = max3f(a, __uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1]));
+    mxc[c] = a;
+  }
+  return max3f(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3]));
+}
+
+// p = 2^(x*scale - mb) for the 128 logits, in packed fp32x2 arithmetic; the
+// bf16 pair k of chunk c overwrites s[c][k] (both of its sources are already
+// consumed).  lsum gets the row sum of p in two packed partial sums.
+__device__ __forceinline__ void exp_pass(uint32_t (&s)[4][32], uint64_t sc2, float mb,
+                                         uint64_t (&lsum)[2]) {
+  const uint64_t nm2 = f2_pack(-mb, -mb);
+  lsum[0] = 0ull;
+  lsum[1] = 0ull;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[c][2 * k]),
+                                         __uint_as_float(s[c][2 * k + 1])), sc2, nm2);
+      float x0, x1;
+      f2_unpack(x2, x0, x1);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      lsum[k & 1] = f2_add(lsum[k & 1], f2_pack(p0, p1));
+      s[c][k] = pack_bf16x2(p0, p1);
+    }
+  }
+}
 
 struct Ring {
   uint32_t stage = 0, phase = 0;
@@ -515,62 +571,59 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
 
         const int kv0 = (item.t0 + jj) * BN;
-        if (kv0 + BN > e_row) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (kv0 + 32 * c + i >= e_row) s[c][i] = __float_as_uint(-INFINITY);
-        }
-        float mxc[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float a = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            a = max3f(a, __uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1]));
-          mxc[c] = a;
-        }
-        const float m_tile = max3f(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3])) * P.scale_log2;
-        const bool need = m_tile > m + RESCALE_LOG2;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? m_tile : m;
-          const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-          if (jj > 0) {
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t o[16];
-              tmem_ld16(tO + 16u * c, o);
-              tmem_ld_wait16(o);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st16(tO + 16u * c, o);
-            }
-          }
-          l *= alpha;
-          m = m_new;
-        }
-        const float mb = (m == -INFINITY) ? 0.f : m;
-        // p = 2^(x*scale - m), pairs in packed fp32x2 arithmetic; the bf16
-        // pair k of chunk c overwrites s[c][k] (both of its sources are
-        // already consumed), then columns 16c..16c+15 of S_t receive
-        // P[32c .. 32c+31].
+        mask_tail(s, kv0, e_row);
+        // Once a row has a max m, the tile's exponentials are taken against
+        // it without looking for the tile max: m only has to keep p finite,
+        // and every p <= the row sum, so a row sum <= 2^64 proves the pass
+        // good (bf16 P has the same relative precision at any magnitude, and
+        // fp32 O and l have range to spare).  A warp whose rows have no max
+        // yet, or whose pass overflowed that bound, takes the exact path:
+        // tile max first, O and l rescaled, exponentials redone.  S is still
+        // intact in TMEM then, because P is stored only after the check.
         const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
-        const uint64_t nm2 = f2_pack(-mb, -mb);
-        uint64_t lsum[2] = {0ull, 0ull};
+        uint64_t lsum[2];
+        bool exact = __any_sync(0xffffffffu, m == -INFINITY);
+        if (!exact) {
+          exp_pass(s, sc2, m, lsum);
+          float a0, a1, b0, b1;
+          f2_unpack(lsum[0], a0, a1);
+          f2_unpack(lsum[1], b0, b1);
+          const float tile_sum = (a0 + a1) + (b0 + b1);
+          if (__any_sync(0xffffffffu, !(tile_sum <= SPEC_SUM_LIMIT))) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s[c]);
+            tmem_ld_wait_only();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
+            mask_tail(s, kv0, e_row);
+            exact = true;
+          }
+        }
+        if (exact) {
+          const float m_tile = tile_max(s) * P.scale_log2;
+          const bool need = m_tile > m + RESCALE_LOG2;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = need ? m_tile : m;
+            const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+            if (jj > 0) {
+#pragma unroll 1
+              for (int c = 0; c < 8; ++c) {
+                uint32_t o[16];
+                tmem_ld16(tO + 16u * c, o);
+                tmem_ld_wait16(o);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st16(tO + 16u * c, o);
+              }
+            }
+            l *= alpha;
+            m = m_new;
+          }
+          exp_pass(s, sc2, (m == -INFINITY) ? 0.f : m, lsum);
+        }
+        // columns 16c..16c+15 of S_t receive P[32c .. 32c+31]
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[c][2 * k]),
-                                               __uint_as_float(s[c][2 * k + 1])), sc2, nm2);
-            float x0, x1;
-            f2_unpack(x2, x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            lsum[k & 1] = f2_add(lsum[k & 1], f2_pack(p0, p1));
-            s[c][k] = pack_bf16x2(p0, p1);
-          }
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) pk[k] = s[c][k];
