@@ -49,7 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[k for k, w in WORKLOADS.items() if w.dtype == "bf16" and not w.prefill])
+                    choices=[k for k, w in WORKLOADS.items() if w.dtype == "bf16"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
@@ -340,12 +340,32 @@ def time_e2e(args, sess: UnitSession, device):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
-def time_hbm_kernels(sess: UnitSession, device, peaks):
-    """Append and Euler alone: each launch bracketed by its own event pair
-    (kernel duration, not host launch gaps), rotating buffer sets whose total
-    is larger than L2 so every launch streams from HBM."""
-    from streaming_block_causal_flash_b300 import ws
+def graph_time_us(launch, reps: int, device) -> float:
+    """Mean device time of one launch among `reps` back-to-back launches,
+    captured once in a CUDA graph and replayed between two CUDA events (no
+    host launch overhead, no event between kernels)."""
+    launch(0, torch.cuda.current_stream(device))           # first call outside capture
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            launch(i, torch.cuda.current_stream(device))
     stream = torch.cuda.current_stream(device)
+    g.replay()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def time_hbm_kernels(sess: UnitSession, device, peaks):
+    """Append and Euler alone, as back-to-back launches replayed from a CUDA
+    graph, rotating buffer sets whose total is 3x larger than L2 so every
+    launch streams from HBM."""
+    from streaming_block_causal_flash_b300 import ws
     w = sess.w
     H, D = w.heads, w.head_dim
     u = sess.units[0]
@@ -356,21 +376,10 @@ def time_hbm_kernels(sess: UnitSession, device, peaks):
     vs = [torch.randn(n, H, D, device=device).to(torch.bfloat16) for _ in range(nsets)]
     cap_sets = max(1, sess.cap // n - 1)
 
-    def timed(launch, reps):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(reps)]
-        for i in range(reps):
-            evs[i][0].record(stream)
-            launch(i)
-            evs[i][1].record(stream)
-        torch.cuda.synchronize(device)
-        return statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3   # us
+    def append(i, st):
+        ws.ws_kv_append(ks[i % nsets], vs[i % nsets], sess.k, sess.v, (i % cap_sets) * n, stream=st)
 
-    def append(i):
-        ws.ws_kv_append(ks[i % nsets], vs[i % nsets], sess.k, sess.v, (i % cap_sets) * n, stream=stream)
-
-    timed(append, nsets)                       # warm-up
-    us = timed(append, 8 * nsets)
+    us = graph_time_us(append, 8 * nsets, device)
     byts = 4.0 * slice_bytes
     out = {"append": {"us": round(us, 2), "bytes": int(byts), "gbs": round(byts / us / 1e3, 1),
                       "frac_hbm": round(byts / us / 1e3 / peaks["hbm_gbs"], 3)}}
@@ -381,16 +390,29 @@ def time_hbm_kernels(sess: UnitSession, device, peaks):
     zs = [torch.randn(nl, device=device) for _ in range(zsets)]
     vls = [torch.randn(nl, device=device).to(torch.bfloat16) for _ in range(zsets)]
 
-    def euler(i):
-        ws.ws_fm_euler_step(zs[i % zsets], vls[i % zsets], 0.25, stream=stream)
+    def euler(i, st):
+        ws.ws_fm_euler_step(zs[i % zsets], vls[i % zsets], 0.25, stream=st)
 
-    timed(euler, zsets)
-    us = timed(euler, 8 * zsets)
+    us = graph_time_us(euler, 8 * zsets, device)
     out["euler"] = {"us": round(us, 2), "bytes": int(per), "gbs": round(per / us / 1e3, 1),
                     "frac_hbm": round(per / us / 1e3 / peaks["hbm_gbs"], 3)}
-    out["method"] = (f"mean of per-launch CUDA-event durations, rotating {nsets} (append) / "
-                     f"{zsets} (Euler) buffer sets larger than L2 in total")
+    out["method"] = (f"back-to-back launches replayed from a CUDA graph, mean per launch; rotating "
+                     f"{nsets} (append) / {zsets} (Euler) buffer sets, 3x L2 in total; "
+                     f"peak = measured HBM copy bandwidth")
     return out
+
+
+def time_unit_graph(sess: UnitSession, device, reps: int = 50):
+    """The whole unit step (append, attention, Euler steps) captured once in a
+    CUDA graph and replayed: per-unit latency without host launch overhead."""
+    u = sess.units[0]
+
+    def step(i, st):
+        run_unit(sess, u, st)
+
+    us = graph_time_us(step, reps, device)
+    return {"us_per_unit": round(us, 1), "value": round(sess.unit_flops(u) / (us * 1e-6) / 1e12, 3),
+            "unit": UNIT, "method": f"{reps} unit steps captured in one CUDA graph, replayed once"}
 
 
 # ------------------------------------------------------------ oracle arms
@@ -460,6 +482,8 @@ def reference_arm(args, rank, world):
     if rank != 0:
         return None
     w = WORKLOADS[args.workload]
+    if w.prefill:
+        raise SystemExit("--impl reference times the oracle on the streaming-unit workloads only")
     sess = UnitSession(w, None, host_only=True)
     u = sess.units[0]
     offs = sess.offsets_all[:u + 2]
@@ -501,6 +525,104 @@ def workload_config(w: Workload, sess: UnitSession, u: int):
                   f"({2 * w.heads * int(offs[-1]) * w.head_dim * 2 / 1e9:.2f} GB)"}
 
 
+# ------------------------------------------------------------ prefill arm
+
+def prefill_main(args, w: Workload, device, rank, world, peaks):
+    """One step = the session prefill: bulk KV append of all T tokens, then
+    full-sequence block-causal attention over them (every call through the C
+    ABI)."""
+    from streaming_block_causal_flash_b300 import ws
+    sizes = w.unit_sizes()
+    offs = w.offsets()
+    T, H, D = int(offs[-1]), w.heads, w.head_dim
+    q_h = w.token_major_range("q", 0, w.n_units, sizes)
+    k_h = w.token_major_range("k", 0, w.n_units, sizes)
+    v_h = w.token_major_range("v", 0, w.n_units, sizes)
+    q, k_new, v_new = q_h.to(device), k_h.to(device), v_h.to(device)
+    kc = torch.empty(H, T, D, dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    out = torch.empty_like(q)
+    offs_dev = torch.from_numpy(offs.astype(np.int32)).to(device)
+    flops = attention_flops(offs, np.arange(T), H, D)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None, st=stream, src=(q, k_new, v_new), dst=out):
+        if ev is not None:
+            ev[0].record(st)
+        ws.ws_kv_append(src[1], src[2], kc, vc, 0, stream=st)
+        if ev is not None:
+            ev[1].record(st)
+        ws.ws_block_causal_prefill(src[0], kc, vc, dst, offs, offs_dev, stream=st)
+        if ev is not None:
+            ev[2].record(st)
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize(device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    clk = clocks.stop()
+    code, info = ws.ws_get_device_error()
+    if code != 0:
+        raise SystemExit(f"device error word set during the timed region: {info:#x}")
+    local_ms = start.elapsed_time(stop) / K
+    max_ms, total_flops = reduce_over_ranks(local_ms, flops * K, world, device)
+    value = total_flops / (max_ms * 1e-3 * K) / 1e12
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(max_ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1)*0.5 bf16 Q/K/V",
+            "config": {"workload": w.name, "heads": H, "head_dim": D, "tokens": T,
+                       "units": w.n_units, "attention_tflop": round(flops / 1e12, 3),
+                       "l2": f"inputs larger than L2 (K/V {2 * H * T * D * 2 / 1e9:.2f} GB)"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                         "kernel": "attn_tc_bf16_kernel, prefill mode (one ws_block_causal_prefill call)",
+                         "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4)},
+            "gpu_launches": 2 * K, "clocks": clk,
+            "kernels_ms_mean": {"kv_append_bulk": round(append_ms, 4), "block_causal_prefill": round(attn_ms, 4)}}
+    if not args.no_e2e and rank == 0:
+        hq, hk, hv = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dv, do = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(out)
+        reps = max(3, min(K, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            step(src=(dq, dk, dv), dst=do)
+            ho.copy_(do, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        e_ms = a.elapsed_time(b) / reps
+        line["e2e"] = {"value": round(flops / (e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                       "ms_per_step": round(e_ms, 3), "steps": reps,
+                       "h2d_bytes_per_step": int(3 * q.numel() * 2), "d2h_bytes_per_step": int(out.numel() * 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world, device)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 # --------------------------------------------------------------------- main
 
 def main(argv=None):
@@ -526,6 +648,8 @@ def main(argv=None):
     init_dist(world, "nccl")
     peaks = load_peaks()
     w = WORKLOADS[args.workload]
+    if w.prefill:
+        return prefill_main(args, w, device, rank, world, peaks)
     sess = UnitSession(w, device)
     clocks = ClockSampler(local)
     clocks.start()
@@ -549,7 +673,8 @@ def main(argv=None):
                 "traffic": recorded_traffic(),
                 "kernel": "attn_tc_bf16_kernel (+ attn_combine_kernel) = one ws_block_causal_attn call",
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
-                if peaks["source"] == "measured" else "fallback 1.8 PFLOP/s"}
+                if peaks["source"] == "measured" else "fallback 1.8 PFLOP/s",
+                "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4)}
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(max_ms, 4),
             "us_per_unit": round(max_ms * 1e3, 1), "higher_is_better": True, "scaling": "weak",
@@ -569,6 +694,7 @@ def main(argv=None):
     if rank == 0:
         if not args.no_hbm:
             line["hbm_kernels"] = time_hbm_kernels(sess, device, peaks)
+            line["graph"] = time_unit_graph(sess, device)
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(sess)
         print(json.dumps(line), flush=True)
