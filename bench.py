@@ -39,6 +39,7 @@ DEFAULT_WORKLOAD = "unit_640x368"
 L2_BYTES = 126 * 1024 * 1024
 ATTN_SOURCE = os.path.join(ROOT, "streaming_block_causal_flash_b300", "csrc", "attn_tcgen05.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_tcgen05_unit_640x368_traffic.txt")
+TRAFFIC_WORKLOAD = "unit_640x368"
 
 
 # ----------------------------------------------------------------- plumbing
@@ -153,10 +154,11 @@ def source_digest(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(workload: str = DEFAULT_WORKLOAD):
     """DRAM bytes per attention launch from the committed ncu summary, or None
-    when the kernel source changed since those counters were taken."""
-    if not os.path.exists(TRAFFIC_FILE):
+    when the kernel source changed since those counters were taken or the
+    summary covers another workload."""
+    if workload != TRAFFIC_WORKLOAD or not os.path.exists(TRAFFIC_FILE):
         return None
     vals = {}
     with open(TRAFFIC_FILE) as f:
@@ -396,6 +398,15 @@ def time_hbm_kernels(sess: UnitSession, device, peaks):
     us = graph_time_us(euler, 8 * zsets, device)
     out["euler"] = {"us": round(us, 2), "bytes": int(per), "gbs": round(per / us / 1e3, 1),
                     "frac_hbm": round(per / us / 1e3 / peaks["hbm_gbs"], 3)}
+    vcs = [torch.randn(nl, device=device).to(torch.bfloat16) for _ in range(zsets)]
+
+    def euler_cfg(i, st):
+        ws.ws_fm_euler_cfg_step(zs[i % zsets], vls[i % zsets], vcs[(i + 1) % zsets], 3.0, 0.25, stream=st)
+
+    us = graph_time_us(euler_cfg, 8 * zsets, device)
+    per_cfg = nl * (4 + 2 + 2 + 4)
+    out["euler_cfg"] = {"us": round(us, 2), "bytes": int(per_cfg), "gbs": round(per_cfg / us / 1e3, 1),
+                        "frac_hbm": round(per_cfg / us / 1e3 / peaks["hbm_gbs"], 3)}
     out["method"] = (f"back-to-back launches replayed from a CUDA graph, mean per launch; rotating "
                      f"{nsets} (append) / {zsets} (Euler) buffer sets, 3x L2 in total; "
                      f"peak = measured HBM copy bandwidth")
@@ -670,7 +681,7 @@ def main(argv=None):
     achieved = per_launch / (attn_avg_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": recorded_traffic(),
+                "traffic": recorded_traffic(w.name),
                 "kernel": "attn_tc_bf16_kernel (+ attn_combine_kernel) = one ws_block_causal_attn call",
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
                 if peaks["source"] == "measured" else "fallback 1.8 PFLOP/s",

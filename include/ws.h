@@ -193,6 +193,28 @@ WS_API ws_status ws_block_causal_attn_noalloc(const void* q, const void* k_cache
                                               ws_stream_t stream);
 
 /*
+ * ws_fm_euler_cfg_step -- one Euler step with a classifier-free-guided
+ * velocity, in one pass over memory.  [close-read] 五、训练 item 3: the
+ * low-latency student is distilled from a teacher that samples with CFG and
+ * more solver steps; the pages give no formula, and the standard guidance
+ * combination is taken:
+ *   v = v_uncond + guidance * (v_cond - v_uncond),   z <- z - dtau * v
+ * in fp32 as d = v_cond - v_uncond, v = fma(guidance, d, v_uncond),
+ * z = fma(-dtau, v, z).  guidance 0 / 1 give the unconditional / conditional
+ * step.
+ *
+ * z                  device, n_elems float32 (z_dt must be WS_F32), in place
+ * v_uncond, v_cond   device, n_elems values of dtype v_dt (WS_BF16 or WS_F32)
+ * z_bf16_out_or_null device bf16 [n_elems] receiving the new z rounded to
+ *                    bf16, or NULL
+ * Errors as ws_fm_euler_step; guidance must be finite.
+ */
+WS_API ws_status ws_fm_euler_cfg_step(void* z, ws_dtype z_dt, const void* v_uncond,
+                                      const void* v_cond, ws_dtype v_dt, void* z_bf16_out_or_null,
+                                      int64_t n_elems, float guidance, float dtau,
+                                      ws_stream_t stream);
+
+/*
  * Bytes of workspace ws_block_causal_attn needs for these sizes on the
  * current device (0 when no key range is split).  Returns SIZE_MAX when the
  * sizes are invalid or the device cannot be queried.

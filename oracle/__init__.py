@@ -35,7 +35,10 @@ Functions and what pins each (tests/test_oracle_pins.py):
   at a time rebuilds the timeline; bytes outside the written range unchanged.
 * ``flow_matching`` -- closed form: one Euler step from tau=1 with the exact
   velocity recovers z_0; uniform k-step solve also recovers z_0; one step of
-  any size moves along the straight interpolant exactly.
+  any size moves along the straight interpolant exactly.  Guided step: w = 0
+  and w = 1 give the unconditional and conditional steps exactly; with both
+  velocities equal to the exact one, any w recovers z_0; the guided velocity
+  is affine in w (two-point extrapolation).
 
 No function here is "parity unpinned".
 """

@@ -12,6 +12,14 @@ published (same page 七、局限 4); the reading taken here is the plain Euler
 method on a uniform grid from tau = 1 down to tau = 0:
     z_{tau - dtau} = z_tau - dtau * v(z_tau, tau).
 All arithmetic is fp64; callers round once to their own dtype to compare.
+
+Classifier-free guidance: the same page (五、训练, item 3) says the
+low-latency student is distilled from a teacher that samples with CFG and
+more solver steps.  The pages give no formula; the reading taken here is the
+standard guidance combination applied to the velocity,
+    v = v_uncond + w * (v_cond - v_uncond),
+followed by the same Euler update.  w = 0 gives the unconditional velocity,
+w = 1 the conditional one.
 """
 from __future__ import annotations
 
@@ -49,3 +57,15 @@ def euler_solve(z1, velocity_fn, n_steps: int):
     for a, b in zip(grid[:-1], grid[1:]):
         z = euler_step(z, velocity_fn(z, a), a - b)
     return z
+
+
+def cfg_velocity(v_uncond, v_cond, w: float):
+    """Guided velocity v_uncond + w * (v_cond - v_uncond)."""
+    vu = np.asarray(v_uncond, dtype=np.float64)
+    vc = np.asarray(v_cond, dtype=np.float64)
+    return vu + float(w) * (vc - vu)
+
+
+def cfg_euler_step(z, v_uncond, v_cond, w: float, dtau: float):
+    """One Euler step with the guided velocity: z - dtau * cfg_velocity."""
+    return euler_step(z, cfg_velocity(v_uncond, v_cond, w), dtau)

@@ -312,6 +312,28 @@ ws_status ws_fm_euler_step(void* z, ws_dtype z_dt, const void* v, ws_dtype v_dt,
   return ok();
 }
 
+ws_status ws_fm_euler_cfg_step(void* z, ws_dtype z_dt, const void* v_uncond, const void* v_cond,
+                               ws_dtype v_dt, void* z_bf16_out_or_null, int64_t n_elems,
+                               float guidance, float dtau, ws_stream_t stream) {
+  const char* who = "ws_fm_euler_cfg_step";
+  if (z_dt != WS_F32) return fail(WS_ERR_UNSUPPORTED, "%s: z must be float32", who);
+  if (!valid_dtype(v_dt)) return fail(WS_ERR_INVALID_ARGUMENT, "%s: unknown velocity dtype", who);
+  if (n_elems < 0) return fail(WS_ERR_INVALID_ARGUMENT, "%s: negative n_elems", who);
+  if (!std::isfinite(dtau) || !std::isfinite(guidance))
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: dtau and guidance must be finite", who);
+  if (n_elems == 0) return ok();
+  if (!z || !v_uncond || !v_cond) return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer argument", who);
+  if (!aligned16(z) || !aligned16(v_uncond) || !aligned16(v_cond) ||
+      (z_bf16_out_or_null && !aligned16(z_bf16_out_or_null)))
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: pointers must be 16-byte aligned", who);
+  const int sms = device_sms(nullptr);
+  if (sms <= 0) return fail(WS_ERR_CUDA, "%s: cannot query the current device", who);
+  cudaError_t e = ws::launch_fm_euler_cfg(static_cast<float*>(z), v_uncond, v_cond, v_dt == WS_BF16,
+                                          z_bf16_out_or_null, n_elems, guidance, dtau, sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  return ok();
+}
+
 size_t ws_block_causal_attn_workspace_size(int64_t q_len, int64_t kv_len, int num_heads,
                                            int head_dim) {
   if (q_len < 0 || kv_len < q_len || num_heads < 1 || head_dim < 1 || kv_len > INT32_MAX)

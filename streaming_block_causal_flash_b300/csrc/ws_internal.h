@@ -20,6 +20,9 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
 // ---- Flow-matching Euler step (fm_euler.cu)
 cudaError_t launch_fm_euler(float* z, const void* v, bool v_is_bf16, void* z_bf16_out,
                             int64_t n, float dtau, int num_sms, cudaStream_t s);
+cudaError_t launch_fm_euler_cfg(float* z, const void* v_uncond, const void* v_cond, bool v_is_bf16,
+                                void* z_bf16_out, int64_t n, float guidance, float dtau,
+                                int num_sms, cudaStream_t s);
 
 // ---- fp32 SIMT attention (attn_simt.cu)
 struct SimtAttnArgs {

@@ -42,6 +42,7 @@ SIGNATURES = {
     "ws_block_causal_attn_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _i32p, _vp, _c_int, _c_i64,
                                               _c_int, _c_int, _c_f32, _c_int, _vp]),
     "ws_fm_euler_step": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _c_i64, _c_f32, _vp]),
+    "ws_fm_euler_cfg_step": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _vp, _c_i64, _c_f32, _c_f32, _vp]),
     "ws_block_causal_attn_workspace_size": (_c_size, [_c_i64, _c_i64, _c_int, _c_int]),
     "ws_status_string": (ctypes.c_char_p, [_c_int]),
     "ws_last_error": (ctypes.c_char_p, []),
@@ -209,6 +210,23 @@ def ws_fm_euler_step(z: torch.Tensor, v: torch.Tensor, dtau: float,
     _check(load().ws_fm_euler_step(_dev(z, "z"), _dtype_code(z), _dev(v, "v"), _dtype_code(v),
                                    _dev(z_bf16_out, "z_bf16_out", torch.bfloat16), int(z.numel()),
                                    float(dtau), _stream_ptr(stream)))
+
+
+def ws_fm_euler_cfg_step(z: torch.Tensor, v_uncond: torch.Tensor, v_cond: torch.Tensor,
+                         guidance: float, dtau: float, z_bf16_out: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    """z <- z - dtau * (v_u + guidance * (v_c - v_u)) in place (z float32)."""
+    if not (z.numel() == v_uncond.numel() == v_cond.numel()):
+        raise ValueError("z and the velocities differ in size")
+    if v_uncond.dtype != v_cond.dtype:
+        raise TypeError("v_uncond and v_cond must share a dtype")
+    if z_bf16_out is not None and z_bf16_out.numel() != z.numel():
+        raise ValueError("z_bf16_out size mismatch")
+    _check(load().ws_fm_euler_cfg_step(_dev(z, "z"), _dtype_code(z), _dev(v_uncond, "v_uncond"),
+                                       _dev(v_cond, "v_cond"), _dtype_code(v_uncond),
+                                       _dev(z_bf16_out, "z_bf16_out", torch.bfloat16),
+                                       int(z.numel()), float(guidance), float(dtau),
+                                       _stream_ptr(stream)))
 
 
 def ws_block_causal_attn_workspace_size(q_len: int, kv_len: int, num_heads: int,

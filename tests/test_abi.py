@@ -96,6 +96,16 @@ def test_euler_host_validation(lib):
     assert lib.ws_fm_euler_step(0, ws.WS_F32, 0, ws.WS_BF16, None, 0, 0.25, None) == ws.WS_OK
 
 
+def test_euler_cfg_host_validation(lib):
+    f = lib.ws_fm_euler_cfg_step
+    assert f(FAKE, ws.WS_BF16, FAKE, FAKE, ws.WS_BF16, None, 8, 2.0, 0.25, None) == ws.WS_ERR_UNSUPPORTED
+    assert f(FAKE, ws.WS_F32, FAKE, FAKE + 4, ws.WS_BF16, None, 8, 2.0, 0.25, None) == ws.WS_ERR_INVALID_ARGUMENT
+    assert f(FAKE, ws.WS_F32, FAKE, FAKE, ws.WS_BF16, None, 8, float("nan"), 0.25, None) == \
+        ws.WS_ERR_INVALID_ARGUMENT
+    assert f(FAKE, ws.WS_F32, 0, FAKE, ws.WS_BF16, None, 8, 2.0, 0.25, None) == ws.WS_ERR_INVALID_ARGUMENT
+    assert f(0, ws.WS_F32, 0, 0, ws.WS_BF16, None, 0, 2.0, 0.25, None) == ws.WS_OK
+
+
 def test_timeout_setting_rejects_zero(lib):
     assert lib.ws_set_wait_timeout_ns(0) == ws.WS_ERR_INVALID_ARGUMENT
     assert lib.ws_set_wait_timeout_ns(2_000_000_000) == ws.WS_OK

@@ -56,6 +56,7 @@ def test_recorded_traffic_is_null_when_kernel_changed(tmp_path, monkeypatch):
     assert bench.recorded_traffic() is None
     f.write_text(f"dram_bytes_per_launch: 123\nkernel_source_sha256_16: {bench.source_digest(bench.ATTN_SOURCE)}\n")
     assert bench.recorded_traffic() == 123.0
+    assert bench.recorded_traffic("long_session_640x368") is None
 
 
 def test_clock_sampler_without_nvidia_smi(monkeypatch):

@@ -71,6 +71,43 @@ def test_euler_exact_velocity_recovers_z0_in_four_steps():
     np.testing.assert_allclose(z.cpu().numpy(), z0.numpy(), rtol=0, atol=1e-5)
 
 
+@pytest.mark.parametrize("guidance", [0.0, 1.0, 3.0])
+def test_euler_cfg_four_bf16_steps(guidance):
+    """Guided step against the oracle.  Bound from the fp32 arithmetic: per
+    step the kernel rounds d = v_c - v_u, v = fma(w, d, v_u) and
+    z = fma(-dtau, v, z) once each, an error of at most
+    2^-24 (|z| + dtau (|v| + |w| |d|)) per step (taken as 2^-23 for margin),
+    accumulated over the steps.  The bf16 copy must be the exact
+    round-to-nearest-even image of the fp32 result."""
+    w = WORKLOADS["unit_640x368"]
+    n = w.latent_tokens * w.latent_channels + 5
+    z_init = normal(7, "z_cfg", 0, (n,))
+    vus = [normal(7, "vu", s, (n,), 1.0, torch.bfloat16) for s in range(4)]
+    vcs = [normal(7, "vc", s, (n,), 1.0, torch.bfloat16) for s in range(4)]
+    z = z_init.clone().cuda()
+    zb = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    ref = z_init.numpy().astype(np.float64)
+    bound = 0.0
+    for s in range(4):
+        ws.ws_fm_euler_cfg_step(z, vus[s].cuda(), vcs[s].cuda(), guidance, 0.25, z_bf16_out=zb)
+        vu, vc = vus[s].float().numpy(), vcs[s].float().numpy()
+        v = fm.cfg_velocity(vu, vc, guidance)
+        ref = fm.cfg_euler_step(ref, vu, vc, guidance, 0.25)
+        bound += 2.0 ** -23 * (np.abs(ref).max() + 0.25 * (np.abs(v).max() + abs(guidance) * np.abs(vc - vu).max()))
+        got = z.cpu().numpy().astype(np.float64)
+        assert_close_abs(got, ref, bound, f"guided step {s}")
+        assert torch.equal(zb.cpu(), z.cpu().to(torch.bfloat16)), "bf16 copy"
+
+
+def test_euler_cfg_with_exact_velocity_recovers_z0():
+    w = WORKLOADS["unit_192x336"]
+    z0, eps = w.z0(3), w.eps(3)
+    v = (eps - z0).cuda()
+    z = eps.clone().cuda()
+    ws.ws_fm_euler_cfg_step(z, v, v, 2.5, 1.0)
+    np.testing.assert_allclose(z.cpu().numpy(), z0.numpy(), rtol=0, atol=F32_ABS)
+
+
 # ----------------------------------------------------------------- KV append
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "unit_192x336", "unit_640x368"])

@@ -265,6 +265,36 @@ def test_single_step_moves_along_the_straight_path():
         np.testing.assert_allclose(z, fm.interpolant(z0, eps, tau - dtau), rtol=0, atol=1e-14)
 
 
+def test_cfg_endpoints_are_the_plain_velocities():
+    rng = np.random.default_rng(11)
+    vu, vc, z = rng.standard_normal((3, 6, 5))
+    # w = 0 is exact; w = 1 computes v_u + (v_c - v_u), equal to v_c up to one
+    # fp64 rounding of the difference
+    np.testing.assert_array_equal(fm.cfg_velocity(vu, vc, 0.0), vu)
+    np.testing.assert_allclose(fm.cfg_velocity(vu, vc, 1.0), vc, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(fm.cfg_euler_step(z, vu, vc, 0.0, 0.25), fm.euler_step(z, vu, 0.25))
+    np.testing.assert_allclose(fm.cfg_euler_step(z, vu, vc, 1.0, 0.25), fm.euler_step(z, vc, 0.25),
+                               rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("w", [0.0, 1.0, 3.5, -2.0])
+def test_cfg_with_exact_velocity_recovers_z0_for_any_guidance(w):
+    # both branches predict the exact velocity eps - z0: guidance changes nothing
+    rng = np.random.default_rng(12)
+    z0, eps = rng.standard_normal((2, 16, 64))
+    v = fm.velocity(z0, eps)
+    z = fm.interpolant(z0, eps, 1.0)
+    np.testing.assert_allclose(fm.cfg_euler_step(z, v, v, w, 1.0), z0, rtol=0, atol=1e-14)
+
+
+def test_cfg_velocity_is_affine_in_guidance():
+    # v(w) on the line through v(0) = v_u and v(1) = v_c: v(w) = (1 - w) v_u + w v_c
+    rng = np.random.default_rng(13)
+    vu, vc = rng.standard_normal((2, 7, 3))
+    for w in (-1.5, 0.25, 2.0, 7.5):
+        np.testing.assert_allclose(fm.cfg_velocity(vu, vc, w), (1 - w) * vu + w * vc, rtol=0, atol=1e-12)
+
+
 def test_uniform_grid():
     assert np.allclose(fm.uniform_grid(4), [1.0, 0.75, 0.5, 0.25, 0.0])
 
@@ -298,6 +328,15 @@ def test_planted_mistake_euler_sign_is_caught(monkeypatch):
                         lambda z, v, dtau: np.asarray(z, np.float64) + dtau * np.asarray(v, np.float64))
     with pytest.raises(AssertionError):
         test_one_euler_step_from_noise_recovers_clean_latent_exactly()
+
+
+def test_planted_mistake_cfg_swapped_branches_is_caught(monkeypatch):
+    # a guidance combination that swaps the branches fails the endpoint pin
+    rng = np.random.default_rng(14)
+    vu, vc = rng.standard_normal((2, 4, 4))
+    monkeypatch.setattr(fm, "cfg_velocity", lambda a, b, w: np.asarray(b) + w * (np.asarray(a) - np.asarray(b)))
+    with pytest.raises(AssertionError):
+        np.testing.assert_array_equal(fm.cfg_velocity(vu, vc, 0.0), vu)
 
 
 def test_planted_mistake_dropped_normalisation_is_caught(monkeypatch):
