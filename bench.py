@@ -413,6 +413,26 @@ def time_hbm_kernels(sess: UnitSession, device, peaks):
     return out
 
 
+def time_attn_side(sess: UnitSession, device, peaks, reps: int = 20):
+    """ws_block_causal_attn_side for the unit (history from the cache, the
+    unit's own K/V from its slice buffers), graph-replayed back to back."""
+    from streaming_block_causal_flash_b300 import ws
+    u = sess.units[0]
+    n = sess.sizes[u]
+    offs = sess.offsets_all[:u + 2]
+    k_side, v_side = sess.kv[u]
+
+    def call(i, st):
+        ws.ws_block_causal_attn_side(sess.q[u], sess.k, sess.v, k_side, v_side, sess.out[:n], offs,
+                                     sess.offs_dev[u], workspace=sess.workspace, stream=st)
+
+    us = graph_time_us(call, reps, device)
+    achieved = sess.unit_flops(u) / (us * 1e-6) / 1e12
+    return {"us": round(us, 1), "achieved": round(achieved, 2), "unit": "TFLOP/s",
+            "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "method": f"{reps} calls replayed from a CUDA graph"}
+
+
 def time_unit_graph(sess: UnitSession, device, reps: int = 50):
     """The whole unit step (append, attention, Euler steps) captured once in a
     CUDA graph and replayed: per-unit latency without host launch overhead."""
@@ -706,6 +726,7 @@ def main(argv=None):
         if not args.no_hbm:
             line["hbm_kernels"] = time_hbm_kernels(sess, device, peaks)
             line["graph"] = time_unit_graph(sess, device)
+            line["attn_side"] = time_attn_side(sess, device, peaks)
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(sess)
         print(json.dumps(line), flush=True)

@@ -119,6 +119,36 @@ WS_API ws_status ws_block_causal_attn(const void* q, const void* k_cache, const 
                                void* workspace, size_t workspace_bytes, ws_stream_t stream);
 
 /*
+ * ws_block_causal_attn_side -- ws_block_causal_attn with the newest block's
+ * keys and values read from side buffers instead of the cache.
+ * [close-read] 四、推理 step 3 and [explainer] "点开看部署细节": the performer
+ * runs the flow solver for the next unit over the full-history cache, and
+ * the clean latents are committed to history only once denoised.  While the
+ * solver iterates, the unit's own K/V change every step; they live in side
+ * buffers, and only the final slice is committed with ws_kv_append.
+ *
+ * Same result as ws_kv_append(k_side, v_side, ..., cache_len =
+ * offsets[n_blocks-1]) followed by ws_block_causal_attn, without touching the
+ * cache: every query row of the last block sees the cache keys
+ * j < offsets[n_blocks-1] and all q_len side keys.
+ *
+ * k_side, v_side  device, [q_len][num_heads][head_dim] token-major (the same
+ *                 layout as a slice for ws_kv_append), dtype dt
+ * The cache must hold blocks 0..n_blocks-2 (offsets[n_blocks-1] <= capacity,
+ * else WS_ERR_CAPACITY); rows from offsets[n_blocks-1] on are not read.
+ * Other arguments, the workspace (same size query) and errors as
+ * ws_block_causal_attn.  Implemented for WS_BF16 with head_dim 128 (other
+ * combinations return WS_ERR_UNSUPPORTED).
+ */
+WS_API ws_status ws_block_causal_attn_side(const void* q, const void* k_cache, const void* v_cache,
+                                           const void* k_side, const void* v_side, void* out,
+                                           float* lse_or_null, const int32_t* h_offsets,
+                                           const int32_t* d_offsets, int n_blocks,
+                                           int64_t capacity, int num_heads, int head_dim,
+                                           float softmax_scale, ws_dtype dt, void* workspace,
+                                           size_t workspace_bytes, ws_stream_t stream);
+
+/*
  * ws_block_causal_prefill -- full-sequence block-causal attention over all
  * T = offsets[n_blocks] tokens (the session prefill before streaming;
  * [explainer] "点开看部署细节").  Row i sees keys j < e(i), where e(i) is the
@@ -215,8 +245,9 @@ WS_API ws_status ws_fm_euler_cfg_step(void* z, ws_dtype z_dt, const void* v_unco
                                       ws_stream_t stream);
 
 /*
- * Bytes of workspace ws_block_causal_attn needs for these sizes on the
- * current device (0 when no key range is split).  Returns SIZE_MAX when the
+ * Bytes of workspace ws_block_causal_attn (and ws_block_causal_attn_side)
+ * needs for these sizes on the current device (0 when no key range is
+ * split).  Returns SIZE_MAX when the
  * sizes are invalid or the device cannot be queried.
  */
 WS_API size_t ws_block_causal_attn_workspace_size(int64_t q_len, int64_t kv_len, int num_heads,

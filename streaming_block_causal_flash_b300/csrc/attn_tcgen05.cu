@@ -118,6 +118,10 @@ struct Params {
   int prefill;
   int heads, q_len, q_row0, kv_len, n_blocks;
   int pairs, kv_tiles, groups;
+  // Side mode (unit mode only): keys [0, cache_len) come from the cache, in
+  // kv_tiles_c tiles; the newest block's n_side keys come from the
+  // token-major side buffers, in the remaining kv_tiles - kv_tiles_c tiles.
+  int side, kv_tiles_c, cache_len, n_side;
   long long work;
   int n_items;
   float scale_log2;
@@ -314,7 +318,9 @@ struct Ring {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params P) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_ks,
+                    const __grid_constant__ CUtensorMap tm_vs, const Params P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -368,6 +374,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
+      if (P.side) {
+        tma_prefetch_map(&tm_ks);
+        tma_prefetch_map(&tm_vs);
+      }
       ItemIter it;
       iter_init(P, it);
       Item item;
@@ -389,7 +399,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         const int n_iter = max(item.n[0], item.n[1]);
         for (int j = 0; j < n_iter && ok; ++j) {
-          const int kv0 = (item.t0 + j) * BN;
+          const int tile = item.t0 + j;
+          const bool from_side = P.side && tile >= P.kv_tiles_c;
+          const int kv0 = (from_side ? tile - P.kv_tiles_c : tile) * BN;
           for (int which = 0; which < 2; ++which) {
             if (!wait_bar(bar(BAR_KV_EMPTY + ring.stage), ring.phase ^ 1u, abort_flag,
                           P.timeout_ns, W_PROD_KVE)) {
@@ -398,10 +410,18 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             const uint32_t full = bar(BAR_KV_FULL + ring.stage);
             mbar_arrive_expect_tx(full, TILE_BYTES);
-            const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(sKV + ring.stage * TILE_BYTES + hf * HALF_BYTES, map, full, hf * 64, kv0,
-                          item.h);
+            if (from_side) {
+              // side buffer [n_side][H*D]: 128 keys x 64 columns of head h
+              const CUtensorMap* map = which == 0 ? &tm_ks : &tm_vs;
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_2d(sKV + ring.stage * TILE_BYTES + hf * HALF_BYTES, map, full,
+                            item.h * HD + hf * 64, kv0);
+            } else {
+              const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_3d(sKV + ring.stage * TILE_BYTES + hf * HALF_BYTES, map, full, hf * 64,
+                            kv0, item.h);
+            }
             ++issued;
             ring.advance();
           }
@@ -570,8 +590,18 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
 
-        const int kv0 = (item.t0 + jj) * BN;
-        mask_tail(s, kv0, e_row);
+        // key range of this tile and the limit its columns are masked at
+        const int tile = item.t0 + jj;
+        int kv0 = tile * BN, e_lim = e_row;
+        if (P.side) {
+          if (tile < P.kv_tiles_c) {
+            e_lim = P.cache_len;
+          } else {
+            kv0 = (tile - P.kv_tiles_c) * BN;
+            e_lim = P.n_side;
+          }
+        }
+        mask_tail(s, kv0, e_lim);
         // Once a row has a max m, the tile's exponentials are taken against
         // it without looking for the tile max: m only has to keep p finite,
         // and every p <= the row sum, so a row sum <= 2^64 proves the pass
@@ -595,7 +625,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_ld_wait_only();
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
-            mask_tail(s, kv0, e_row);
+            mask_tail(s, kv0, e_lim);
             exact = true;
           }
         }
@@ -763,7 +793,7 @@ long long host_group_of(long long f, long long work, int groups) {
 }  // namespace
 
 bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0, int kv_len,
-                  int n_blocks, int num_sms) {
+                  int n_blocks, int num_sms, int side_len) {
   p = TcAttnPlan{};
   p.prefill = prefill ? 1 : 0;
   p.heads = heads;
@@ -775,6 +805,13 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
   p.pairs = (p.qtiles + 1) / 2;
   p.kv_tiles = (kv_len + BN - 1) / BN;
   if (q_len <= 0 || kv_len <= 0 || heads <= 0 || num_sms <= 0) return false;
+  if (side_len < 0 || side_len > kv_len || (prefill && side_len > 0)) return false;
+  p.side_len = side_len;
+  if (side_len > 0) {
+    // the cache part and the side part are tiled separately
+    p.kv_tiles_c = (kv_len - side_len + BN - 1) / BN;
+    p.kv_tiles = p.kv_tiles_c + (side_len + BN - 1) / BN;
+  }
   if (prefill) {
     const long long items = static_cast<long long>(heads) * p.pairs;
     if (items > (1LL << 30)) return false;
@@ -804,7 +841,8 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
 
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                const CUtensorMap& tm_v, uint64_t timeout_ns, cudaStream_t s) {
+                                const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
+                                const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -830,6 +868,10 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   P.n_blocks = plan.n_blocks;
   P.pairs = plan.pairs;
   P.kv_tiles = plan.kv_tiles;
+  P.side = plan.side_len > 0 ? 1 : 0;
+  P.kv_tiles_c = plan.kv_tiles_c;
+  P.cache_len = plan.kv_len - plan.side_len;
+  P.n_side = plan.side_len;
   P.groups = plan.groups;
   P.work = plan.work;
   P.n_items = plan.n_items;
@@ -843,7 +885,7 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   }
   P.timeout_ns = timeout_ns;
   P.force_stall = a.force_stall;
-  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, P);
+  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs, P);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (plan.split) {

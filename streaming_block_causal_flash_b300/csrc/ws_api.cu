@@ -90,7 +90,7 @@ ws_status check_attn_args(const char* who, const void* q, const void* k_cache,
                           const void* v_cache, void* out, const float* lse,
                           const int32_t* h_offsets, const int32_t* d_offsets, int n_blocks,
                           int64_t capacity, int num_heads, int head_dim, float softmax_scale,
-                          ws_dtype dt) {
+                          ws_dtype dt, bool side) {
   if (!valid_dtype(dt)) return fail(WS_ERR_INVALID_ARGUMENT, "%s: unknown dtype %d", who, (int)dt);
   if (!q || !k_cache || !v_cache || !out || !h_offsets || !d_offsets)
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer argument", who);
@@ -104,9 +104,12 @@ ws_status check_attn_args(const char* who, const void* q, const void* k_cache,
   for (int b = 0; b < n_blocks; ++b)
     if (h_offsets[b + 1] < h_offsets[b])
       return fail(WS_ERR_INVALID_ARGUMENT, "%s: offsets decrease at block %d", who, b);
-  if ((int64_t)h_offsets[n_blocks] > capacity)
-    return fail(WS_ERR_CAPACITY, "%s: offsets[n_blocks]=%d exceeds capacity %lld", who,
-                h_offsets[n_blocks], (long long)capacity);
+  // The cache holds every block read from it: all of them, or, when the
+  // newest block comes from side buffers, the ones before it.
+  const int cached = side ? n_blocks - 1 : n_blocks;
+  if ((int64_t)h_offsets[cached] > capacity)
+    return fail(WS_ERR_CAPACITY, "%s: offsets[%d]=%d exceeds capacity %lld", who, cached,
+                h_offsets[cached], (long long)capacity);
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: q/k/v/out must be 16-byte aligned", who);
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -122,13 +125,23 @@ ws_status check_attn_args(const char* who, const void* q, const void* k_cache,
 }
 
 ws_status run_attention(const char* who, bool prefill, const void* q, const void* k_cache,
-                        const void* v_cache, void* out, float* lse, const int32_t* h_offsets,
+                        const void* v_cache, const void* k_side, const void* v_side, void* out,
+                        float* lse, const int32_t* h_offsets,
                         const int32_t* d_offsets, int n_blocks, int64_t capacity, int num_heads,
                         int head_dim, float softmax_scale, ws_dtype dt, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
+  const bool side = k_side != nullptr || v_side != nullptr;
   ws_status st = check_attn_args(who, q, k_cache, v_cache, out, lse, h_offsets, d_offsets,
-                                 n_blocks, capacity, num_heads, head_dim, softmax_scale, dt);
+                                 n_blocks, capacity, num_heads, head_dim, softmax_scale, dt, side);
   if (st != WS_OK) return st;
+  if (side) {
+    if (!k_side || !v_side)
+      return fail(WS_ERR_INVALID_ARGUMENT, "%s: k_side and v_side are both required", who);
+    if (!aligned16(k_side) || !aligned16(v_side))
+      return fail(WS_ERR_INVALID_ARGUMENT, "%s: side buffers must be 16-byte aligned", who);
+    if (dt != WS_BF16)
+      return fail(WS_ERR_UNSUPPORTED, "%s: side buffers are implemented for bf16 only", who);
+  }
   const int kv_len = h_offsets[n_blocks];
   const int q_row0 = prefill ? 0 : h_offsets[n_blocks - 1];
   const int q_len = kv_len - q_row0;
@@ -161,7 +174,8 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   const int sms = device_sms(&dev);
   if (sms <= 0) return fail(WS_ERR_CUDA, "%s: cannot query the current device", who);
   ws::TcAttnPlan plan;
-  if (!ws::plan_tc_attn(plan, prefill, num_heads, q_len, q_row0, kv_len, n_blocks, sms))
+  if (!ws::plan_tc_attn(plan, prefill, num_heads, q_len, q_row0, kv_len, n_blocks, sms,
+                        side ? q_len : 0))
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: sizes out of range", who);
   if (plan.workspace_bytes > 0) {
     if (!workspace || workspace_bytes < plan.workspace_bytes)
@@ -170,9 +184,11 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
     if (!aligned16(workspace))
       return fail(WS_ERR_INVALID_ARGUMENT, "%s: workspace must be 16-byte aligned", who);
   }
-  // TMA maps: Q as a 2-D [q_len][H*D] matrix; K and V as 3-D [H][kv_len][D]
-  // views of the [H][capacity][D] caches, so rows >= kv_len read as zeros.
-  CUtensorMap tm_q, tm_k, tm_v;
+  // TMA maps: Q as a 2-D [q_len][H*D] matrix; K and V as 3-D [H][rows][D]
+  // views of the [H][capacity][D] caches, rows = the keys read from the cache
+  // (kv_len, or q_row0 with side buffers), so rows beyond read as zeros; the
+  // side buffers, like Q, as 2-D [q_len][H*D] matrices.
+  CUtensorMap tm_q, tm_k, tm_v, tm_ks, tm_vs;
   const cuuint64_t D = (cuuint64_t)head_dim;
   {
     cuuint64_t dims[2] = {D * (cuuint64_t)num_heads, (cuuint64_t)q_len};
@@ -182,12 +198,25 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
       return fail(WS_ERR_CUDA, "%s: cannot encode the Q tensor map", who);
   }
   {
-    cuuint64_t dims[3] = {D, (cuuint64_t)kv_len, (cuuint64_t)num_heads};
+    // a cache part of 0 rows (first unit, side mode) still needs a valid map
+    const int rows = side ? (q_row0 > 0 ? q_row0 : 1) : kv_len;
+    cuuint64_t dims[3] = {D, (cuuint64_t)rows, (cuuint64_t)num_heads};
     cuuint64_t strides[2] = {D * 2, (cuuint64_t)capacity * D * 2};
     cuuint32_t box[3] = {64, 128, 1};
     if (!encode_bf16(&tm_k, k_cache, 3, dims, strides, box) ||
         !encode_bf16(&tm_v, v_cache, 3, dims, strides, box))
       return fail(WS_ERR_CUDA, "%s: cannot encode the K/V tensor maps", who);
+  }
+  if (side) {
+    cuuint64_t dims[2] = {D * (cuuint64_t)num_heads, (cuuint64_t)q_len};
+    cuuint64_t strides[1] = {D * (cuuint64_t)num_heads * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (!encode_bf16(&tm_ks, k_side, 2, dims, strides, box) ||
+        !encode_bf16(&tm_vs, v_side, 2, dims, strides, box))
+      return fail(WS_ERR_CUDA, "%s: cannot encode the side-buffer tensor maps", who);
+  } else {
+    tm_ks = tm_k;    // unused without side buffers
+    tm_vs = tm_v;
   }
   ws::TcAttnArgs a{};
   a.q = q;
@@ -200,7 +229,7 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   a.scale = scale;
   a.workspace = workspace;
   a.force_stall = g_force_stall;
-  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, g_timeout_ns, stream);
+  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs, g_timeout_ns, stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
 }
@@ -277,7 +306,8 @@ ws_status ws_block_causal_attn(const void* q, const void* k_cache, const void* v
                                const int32_t* d_offsets, int n_blocks, int64_t capacity,
                                int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
                                void* workspace, size_t workspace_bytes, ws_stream_t stream) {
-  return run_attention("ws_block_causal_attn", false, q, k_cache, v_cache, out, lse_or_null,
+  return run_attention("ws_block_causal_attn", false, q, k_cache, v_cache, nullptr, nullptr, out,
+                       lse_or_null,
                        h_offsets, d_offsets, n_blocks, capacity, num_heads, head_dim,
                        softmax_scale, dt, workspace, workspace_bytes, stream);
 }
@@ -287,7 +317,22 @@ ws_status ws_block_causal_prefill(const void* q, const void* k_cache, const void
                                   const int32_t* d_offsets, int n_blocks, int64_t capacity,
                                   int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
                                   void* workspace, size_t workspace_bytes, ws_stream_t stream) {
-  return run_attention("ws_block_causal_prefill", true, q, k_cache, v_cache, out, lse_or_null,
+  return run_attention("ws_block_causal_prefill", true, q, k_cache, v_cache, nullptr, nullptr, out,
+                       lse_or_null,
+                       h_offsets, d_offsets, n_blocks, capacity, num_heads, head_dim,
+                       softmax_scale, dt, workspace, workspace_bytes, stream);
+}
+
+ws_status ws_block_causal_attn_side(const void* q, const void* k_cache, const void* v_cache,
+                                    const void* k_side, const void* v_side, void* out,
+                                    float* lse_or_null, const int32_t* h_offsets,
+                                    const int32_t* d_offsets, int n_blocks, int64_t capacity,
+                                    int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
+                                    void* workspace, size_t workspace_bytes, ws_stream_t stream) {
+  const char* who = "ws_block_causal_attn_side";
+  if (!k_side || !v_side)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: k_side and v_side are required", who);
+  return run_attention(who, false, q, k_cache, v_cache, k_side, v_side, out, lse_or_null,
                        h_offsets, d_offsets, n_blocks, capacity, num_heads, head_dim,
                        softmax_scale, dt, workspace, workspace_bytes, stream);
 }
@@ -341,11 +386,16 @@ size_t ws_block_causal_attn_workspace_size(int64_t q_len, int64_t kv_len, int nu
   if (head_dim != 128 || q_len == 0) return 0;
   const int sms = device_sms(nullptr);
   if (sms <= 0) return SIZE_MAX;
-  ws::TcAttnPlan plan;
-  if (!ws::plan_tc_attn(plan, false, num_heads, (int)q_len, (int)(kv_len - q_len), (int)kv_len, 1,
-                        sms))
-    return SIZE_MAX;
-  return plan.workspace_bytes;
+  // large enough for ws_block_causal_attn and for ws_block_causal_attn_side
+  size_t need = 0;
+  for (int side = 0; side < 2; ++side) {
+    ws::TcAttnPlan plan;
+    if (!ws::plan_tc_attn(plan, false, num_heads, (int)q_len, (int)(kv_len - q_len), (int)kv_len, 1,
+                          sms, side ? (int)q_len : 0))
+      return SIZE_MAX;
+    if (plan.workspace_bytes > need) need = plan.workspace_bytes;
+  }
+  return need;
 }
 
 ws_status ws_get_device_error(int* code_out, int* info_out) {

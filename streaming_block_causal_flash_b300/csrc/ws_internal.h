@@ -61,10 +61,12 @@ struct TcAttnPlan {
   int grid;          // CTAs launched
   bool split;        // unit mode: some head's key range spans several groups
   size_t workspace_bytes;
+  int side_len;      // unit mode: keys of the newest block read from side buffers (0: none)
+  int kv_tiles_c;    // side mode: key tiles of the cache part
 };
 // Fills the plan for the given sizes; returns false when the sizes do not fit.
 bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0, int kv_len,
-                  int n_blocks, int num_sms);
+                  int n_blocks, int num_sms, int side_len = 0);
 
 struct TcAttnArgs {
   const void* q;
@@ -80,7 +82,8 @@ struct TcAttnArgs {
 };
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                const CUtensorMap& tm_v, uint64_t timeout_ns, cudaStream_t s);
+                                const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
+                                const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s);
 cudaError_t read_attn_device_error(int* code, int* info);
 cudaError_t clear_attn_device_error();
 

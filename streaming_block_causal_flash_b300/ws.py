@@ -39,6 +39,8 @@ SIGNATURES = {
                                       _c_int, _c_f32, _c_int, _vp, _c_size, _vp]),
     "ws_block_causal_prefill": (_c_int, [_vp, _vp, _vp, _vp, _vp, _i32p, _vp, _c_int, _c_i64, _c_int,
                                          _c_int, _c_f32, _c_int, _vp, _c_size, _vp]),
+    "ws_block_causal_attn_side": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32p, _vp, _c_int, _c_i64,
+                                           _c_int, _c_int, _c_f32, _c_int, _vp, _c_size, _vp]),
     "ws_block_causal_attn_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _i32p, _vp, _c_int, _c_i64,
                                               _c_int, _c_int, _c_f32, _c_int, _vp]),
     "ws_fm_euler_step": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _c_i64, _c_f32, _vp]),
@@ -168,6 +170,34 @@ def ws_block_causal_attn(q, k_cache, v_cache, out, offsets_host: Sequence[int],
     """Newest unit's queries (the last block) against the whole cache."""
     _attn("ws_block_causal_attn", q, k_cache, v_cache, out, offsets_host, offsets_dev, lse,
           softmax_scale, workspace, stream)
+
+
+def ws_block_causal_attn_side(q, k_cache, v_cache, k_side, v_side, out,
+                              offsets_host: Sequence[int], offsets_dev: torch.Tensor,
+                              lse: Optional[torch.Tensor] = None, softmax_scale: float = 0.0,
+                              workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Newest unit's queries against the cache (blocks before the last) plus
+    the unit's own K/V from token-major side buffers [q_len, H, D]."""
+    H, cap, D = k_cache.shape
+    dt = q.dtype
+    offs = _host_offsets(offsets_host)
+    if offsets_dev.dtype != torch.int32 or offsets_dev.numel() != offs.size:
+        raise ValueError("device offsets must be int32 with the same length as host offsets")
+    if q.dim() != 3 or q.shape[1] != H or q.shape[2] != D or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q/out must be [rows, H, D]")
+    if tuple(k_side.shape) != tuple(q.shape) or tuple(v_side.shape) != tuple(q.shape):
+        raise ValueError("k_side/v_side must be [rows, H, D] like q")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != H * q.shape[0]):
+        raise ValueError("lse must be float32 [H, rows]")
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check(load().ws_block_causal_attn_side(
+        _dev(q, "q"), _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
+        _dev(k_side, "k_side", dt), _dev(v_side, "v_side", dt), _dev(out, "out", dt),
+        _dev(lse, "lse", torch.float32), offs.ctypes.data_as(_i32p),
+        _dev(offsets_dev, "offsets_dev", torch.int32), int(offs.size - 1), int(cap), int(H), int(D),
+        float(softmax_scale), _dtype_code(q), ws_ptr, ws_bytes, _stream_ptr(stream)))
 
 
 def ws_block_causal_attn_noalloc(q, k_cache, v_cache, out, offsets_host: Sequence[int],

@@ -87,6 +87,20 @@ def test_attention_host_validation(lib, fn):
                             ws.WS_BF16, None, 0, None) == ws.WS_ERR_INVALID_ARGUMENT
 
 
+def test_side_attention_host_validation(lib):
+    f = lib.ws_block_causal_attn_side
+
+    def call(offs_vals, ks=FAKE, vs=FAKE, dt=ws.WS_BF16, cap=1024, D=128):
+        arr, p = _offs(offs_vals)
+        return f(FAKE, FAKE, FAKE, ks, vs, FAKE, None, p, FAKE, len(arr) - 1, cap, 2, D, 0.0, dt,
+                 None, 0, None)
+    assert call([0, 8, 16], ks=0) == ws.WS_ERR_INVALID_ARGUMENT          # missing side buffer
+    assert call([0, 8, 16], vs=FAKE + 8) == ws.WS_ERR_INVALID_ARGUMENT   # misaligned side buffer
+    assert call([0, 8, 16], dt=ws.WS_F32) == ws.WS_ERR_UNSUPPORTED        # bf16 only
+    assert call([0, 1100, 1200]) == ws.WS_ERR_CAPACITY                   # history past capacity
+    assert call([0, 9, 5]) == ws.WS_ERR_INVALID_ARGUMENT                 # decreasing offsets
+
+
 def test_euler_host_validation(lib):
     assert lib.ws_fm_euler_step(FAKE, ws.WS_BF16, FAKE, ws.WS_BF16, None, 8, 0.25, None) == ws.WS_ERR_UNSUPPORTED
     assert lib.ws_fm_euler_step(FAKE, ws.WS_F32, FAKE + 4, ws.WS_BF16, None, 8, 0.25, None) == \
