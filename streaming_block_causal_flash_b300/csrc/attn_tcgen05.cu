@@ -744,46 +744,98 @@ __device__ __forceinline__ int group_of(long long f, long long work, int groups)
 }
 
 // Merge the partial results of the groups that share one head:
-//   LSE = log2 sum_s 2^{lse_s},  O = sum_s 2^{lse_s - LSE} O_s.
-// One warp per (query row, head); lane c holds columns 4c..4c+3.
+//   LSE = log2 sum_s 2^{lse_s},  O = sum_s 2^{lse_s - LSE} O_s,
+// as one online pass over the partials (running max, rescaled sum and
+// accumulator).  One block per (head, 32 query rows); the block first lists
+// the partial slots of its head in shared memory (one 64-bit division pair
+// per group, spread over the threads), then each warp merges 4 rows with
+// lane c holding columns 4c..4c+3, issuing the loads of its 4 rows x 2
+// groups together before merging them.
+constexpr int COMBINE_ROWS = 32;
+constexpr int COMBINE_MAX_GROUPS = 1024;
+
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(Params P) {
+  __shared__ int s_gs[COMBINE_MAX_GROUPS];
   const int h = blockIdx.y;
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= P.q_len) return;
   const long long L = P.kv_tiles;
   const int g_lo = group_of(h * L, P.work, P.groups);
   const int g_hi = group_of((h + 1) * L - 1, P.work, P.groups);
   if (g_lo == g_hi) return;   // one group covered the head: final output already written
-  const int pair = row / 256;
-  const int r = row % 256;
-  float mx = -INFINITY;
-  for (int g = g_lo; g <= g_hi; ++g) {
+  const int cnt = g_hi - g_lo + 1;
+  // slot index (partial row block) of group g: (g * pairs + pair) * 2 + slot,
+  // stored without the pair term, which depends on the row
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+    const int g = g_lo + i;
     const int slot = (h == static_cast<int>(group_begin(g, P.work, P.groups) / L)) ? 0 : 1;
-    const size_t prow = (static_cast<size_t>(g * P.pairs + pair) * 2 + slot) * 256 + r;
-    mx = fmaxf(mx, P.ws_lse[prow]);
+    s_gs[i] = g * 2 * P.pairs + slot;
   }
-  float sum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int g = g_lo; g <= g_hi; ++g) {
-    const int slot = (h == static_cast<int>(group_begin(g, P.work, P.groups) / L)) ? 0 : 1;
-    const size_t prow = (static_cast<size_t>(g * P.pairs + pair) * 2 + slot) * 256 + r;
-    const float w = exp2f(P.ws_lse[prow] - mx);
-    sum += w;
-    const float4 o = reinterpret_cast<const float4*>(P.ws_o + prow * HD)[lane];
-    acc.x = fmaf(w, o.x, acc.x);
-    acc.y = fmaf(w, o.y, acc.y);
-    acc.z = fmaf(w, o.z, acc.z);
-    acc.w = fmaf(w, o.w, acc.w);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const float* __restrict__ ws_o = P.ws_o;
+  const float* __restrict__ ws_lse = P.ws_lse;
+  constexpr int RW = COMBINE_ROWS / 8;    // rows per warp
+  constexpr int CB = 2;                    // groups per load batch
+  const int row0 = blockIdx.x * COMBINE_ROWS + warp * RW;
+  float m[RW], sum[RW];
+  float4 acc[RW];
+#pragma unroll
+  for (int k = 0; k < RW; ++k) {
+    m[k] = -INFINITY;
+    sum[k] = 0.f;
+    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  const float inv = 1.f / sum;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(P.out + (static_cast<size_t>(row) * P.heads + h) * HD)[lane] = packed;
-  if (lane == 0 && P.lse != nullptr)
-    P.lse[static_cast<size_t>(h) * P.q_len + row] = (mx + log2f(sum)) * LN2;
+  for (int i0 = 0; i0 < cnt; i0 += CB) {
+    // all loads of this batch (RW rows x 4 groups) before any arithmetic
+    float l[RW][CB];
+    float4 o[RW][CB];
+#pragma unroll
+    for (int k = 0; k < RW; ++k) {
+      const int row = row0 + k;
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {
+        l[k][u] = -INFINITY;
+        o[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row < P.q_len && i0 + u < cnt) {
+          const size_t prow = static_cast<size_t>(s_gs[i0 + u] + 2 * (row >> 8)) * 256 + (row & 255);
+          l[k][u] = ws_lse[prow];
+          o[k][u] = reinterpret_cast<const float4*>(ws_o + prow * HD)[lane];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < RW; ++k) {
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {
+        if (!(l[k][u] > -INFINITY)) continue;   // past cnt, or past q_len
+        if (l[k][u] > m[k]) {
+          const float c = exp2f(m[k] - l[k][u]);   // 0 while m is -inf
+          sum[k] *= c;
+          acc[k].x *= c; acc[k].y *= c; acc[k].z *= c; acc[k].w *= c;
+          m[k] = l[k][u];
+        }
+        const float w = exp2f(l[k][u] - m[k]);
+        sum[k] += w;
+        acc[k].x = fmaf(w, o[k][u].x, acc[k].x);
+        acc[k].y = fmaf(w, o[k][u].y, acc[k].y);
+        acc[k].z = fmaf(w, o[k][u].z, acc[k].z);
+        acc[k].w = fmaf(w, o[k][u].w, acc[k].w);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < RW; ++k) {
+    const int row = row0 + k;
+    if (row >= P.q_len) break;
+    const float inv = 1.f / sum[k];
+    uint2 packed;
+    packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+    packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+    reinterpret_cast<uint2*>(P.out + (static_cast<size_t>(row) * P.heads + h) * HD)[lane] = packed;
+    if (lane == 0 && P.lse != nullptr)
+      P.lse[static_cast<size_t>(h) * P.q_len + row] = (m[k] + log2f(sum[k])) * LN2;
+  }
 }
 
 long long host_group_of(long long f, long long work, int groups) {
@@ -825,6 +877,7 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
   long long g = num_sms / p.pairs;
   if (g < 1) g = 1;
   if (g > p.work) g = p.work;
+  if (g > COMBINE_MAX_GROUPS) g = COMBINE_MAX_GROUPS;   // the merge lists a head's groups in smem
   p.groups = static_cast<int>(g);
   const long long grid = g * p.pairs;
   if (grid > (1LL << 30)) return false;
@@ -889,7 +942,7 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (plan.split) {
-    dim3 grid((plan.q_len + 7) / 8, plan.heads);
+    dim3 grid((plan.q_len + COMBINE_ROWS - 1) / COMBINE_ROWS, plan.heads);
     attn_combine_kernel<<<grid, 256, 0, s>>>(P);
     err = cudaGetLastError();
   }
