@@ -290,56 +290,102 @@ def time_native(args, sess: UnitSession, device, world):
 
 
 def time_e2e(args, sess: UnitSession, device):
-    """Same step through the public API with host buffers: pinned host inputs
-    copied in and results copied out inside the timed region, every step."""
+    """Same step through the public API with host buffers: every step copies
+    its inputs in from pinned host memory and reads its results (O and z)
+    back, inside the timed region.
+
+    Pipelined, as a streaming deployment runs it: two device buffer sets;
+    the inputs of unit k+1 go up on one copy stream and the results of unit
+    k-1 come back on another while unit k computes (buffer reuse guarded by
+    CUDA events).  The plain serial figure (copy in, compute, copy out, one
+    step after another) is reported beside it."""
     from streaming_block_causal_flash_b300 import ws
-    stream = torch.cuda.current_stream(device)
+    compute = torch.cuda.current_stream(device)
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
     w = sess.w
     u = sess.units[0]
     n = sess.sizes[u]
     offs = sess.offsets_all[:u + 2]
     pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
-    h_q, (h_k, h_v) = pin(sess.q_host[u]), tuple(pin(t) for t in sess.kv_host[u])
-    h_vel = [pin(t) for t in sess.vel_host[u]]
-    h_eps = pin(sess.eps_host[u])
-    h_out = torch.empty(n, w.heads, w.head_dim, dtype=torch.bfloat16).pin_memory()
-    h_z = torch.empty_like(h_eps).pin_memory()
-    d_q = torch.empty_like(sess.q[u])
-    d_k, d_v = torch.empty_like(sess.kv[u][0]), torch.empty_like(sess.kv[u][1])
-    d_vel = [torch.empty_like(t) for t in sess.vel[u]]
-    d_z = torch.empty_like(sess.z[u])
-    h2d = sum(t.numel() * t.element_size() for t in [h_q, h_k, h_v, h_eps, *h_vel])
-    d2h = h_out.numel() * h_out.element_size() + h_z.numel() * h_z.element_size()
+    h_in = [pin(sess.q_host[u]), pin(sess.kv_host[u][0]), pin(sess.kv_host[u][1]),
+            pin(sess.eps_host[u])] + [pin(t) for t in sess.vel_host[u]]
+    h_out = [(torch.empty(n, w.heads, w.head_dim, dtype=torch.bfloat16).pin_memory(),
+              torch.empty_like(h_in[3]).pin_memory()) for _ in range(2)]
+    d_in = [[torch.empty(t.shape, dtype=t.dtype, device=device) for t in h_in] for _ in range(2)]
+    d_out = [torch.empty(n, w.heads, w.head_dim, dtype=torch.bfloat16, device=device) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
 
-    def step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        d_z.copy_(h_eps, non_blocking=True)
-        for d, h in zip(d_vel, h_vel):
+    def compute_step(b, st):
+        q, k, v, z, *vel = d_in[b]
+        ws.ws_kv_append(k, v, sess.k, sess.v, int(offs[-2]), stream=st)
+        ws.ws_block_causal_attn(q, sess.k, sess.v, d_out[b], offs, sess.offs_dev[u],
+                                workspace=sess.workspace, stream=st)
+        for s_ in range(w.euler_steps):
+            ws.ws_fm_euler_step(z, vel[s_], 1.0 / w.euler_steps, stream=st)
+
+    def serial_step():
+        for d, h in zip(d_in[0], h_in):
             d.copy_(h, non_blocking=True)
-        ws.ws_kv_append(d_k, d_v, sess.k, sess.v, int(offs[-2]), stream=stream)
-        ws.ws_block_causal_attn(d_q, sess.k, sess.v, sess.out[:n], offs, sess.offs_dev[u],
-                                workspace=sess.workspace, stream=stream)
-        for s in range(w.euler_steps):
-            ws.ws_fm_euler_step(d_z, d_vel[s], 1.0 / w.euler_steps, stream=stream)
-        h_out.copy_(sess.out[:n], non_blocking=True)
-        h_z.copy_(d_z, non_blocking=True)
+        compute_step(0, compute)
+        h_out[0][0].copy_(d_out[0], non_blocking=True)
+        h_out[0][1].copy_(d_in[0][3], non_blocking=True)
 
     steps = max(10, min(args.steps, 100))
     for _ in range(3):
-        step()
+        serial_step()
     torch.cuda.synchronize(device)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(compute)
     for _ in range(steps):
-        step()
-    b.record(stream)
+        serial_step()
+    b.record(compute)
     torch.cuda.synchronize(device)
-    ms = a.elapsed_time(b) / steps
-    return {"value": round(sess.unit_flops(u) / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+    serial_ms = a.elapsed_time(b) / steps
+
+    def pipelined(nsteps, timed):
+        up_done = [torch.cuda.Event() for _ in range(nsteps)]
+        comp_done = [torch.cuda.Event() for _ in range(nsteps)]
+        down_done = [torch.cuda.Event() for _ in range(nsteps)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(compute)
+        up.wait_event(start)
+
+        def upload(i):
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(down_done[i - 2])     # set i%2 free: read back, so computed
+                for d, h in zip(d_in[i % 2], h_in):
+                    d.copy_(h, non_blocking=True)
+                up_done[i].record(up)
+
+        upload(0)
+        for i in range(nsteps):
+            if i + 1 < nsteps:
+                upload(i + 1)
+            compute.wait_event(up_done[i])
+            compute_step(i % 2, compute)
+            comp_done[i].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(comp_done[i])
+                h_out[i % 2][0].copy_(d_out[i % 2], non_blocking=True)
+                h_out[i % 2][1].copy_(d_in[i % 2][3], non_blocking=True)
+                down_done[i].record(down)
+        compute.wait_event(down_done[nsteps - 1])
+        stop.record(compute)
+        torch.cuda.synchronize(device)
+        return start.elapsed_time(stop) / nsteps
+
+    pipelined(4, False)
+    ms = pipelined(steps, True)
+    flops = sess.unit_flops(u)
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "method": "pipelined: inputs of unit k+1 uploaded and results of unit k-1 read back on "
+                      "copy streams while unit k computes; every step moves its own inputs and results",
+            "serial_ms_per_step": round(serial_ms, 4),
+            "serial_value": round(flops / (serial_ms * 1e-3) / 1e12, 3)}
 
 
 def graph_time_us(launch, reps: int, device) -> float:
