@@ -517,7 +517,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           const bool more = jj + 1 < n_iter;
           uint32_t kslot = 0, kphase = 0;
           if (more) { kslot = ring.stage; kphase = ring.phase; ring.advance(); }
-          // every wait and fence of this step before taking the issue lock
+          // every wait and fence of this step before taking the issue lock;
+          // K_{j+1} (normally loaded long before) first, so that only the
+          // wait for this tile's P sits between its softmax and its MMAs
+          if (more && !wait_bar(bar(BAR_KV_FULL + kslot), kphase, abort_flag, P.timeout_ns,
+                                W_MMA_KV)) { ok = false; break; }
           if (jj < n) {
             if (!wait_bar(bar(BAR_P_FULL + t), p_phase, abort_flag, P.timeout_ns, W_MMA_P)) {
               ok = false; break;
@@ -529,8 +533,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               of_phase ^= 1u;
             }
           }
-          if (more && !wait_bar(bar(BAR_KV_FULL + kslot), kphase, abort_flag, P.timeout_ns,
-                                W_MMA_KV)) { ok = false; break; }
           if (jj < n) {
             tc_fence_after();
             if (!issue_lock(issue_lk, abort_flag, P.timeout_ns)) { ok = false; break; }
