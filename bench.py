@@ -479,6 +479,27 @@ def time_attn_side(sess: UnitSession, device, peaks, reps: int = 20):
             "method": f"{reps} calls replayed from a CUDA graph"}
 
 
+def time_fused_unit(sess: UnitSession, device, reps: int = 50):
+    """The unit step with the append fused into the attention: one
+    ws_block_causal_attn_side call that reads the unit's K/V from its slice
+    and commits them to the cache, then the Euler steps; graph-replayed."""
+    from streaming_block_causal_flash_b300 import ws
+    u = sess.units[0]
+    n = sess.sizes[u]
+    offs = sess.offsets_all[:u + 2]
+    k_side, v_side = sess.kv[u]
+
+    def step(i, st):
+        ws.ws_block_causal_attn_side(sess.q[u], sess.k, sess.v, k_side, v_side, sess.out[:n], offs,
+                                     sess.offs_dev[u], workspace=sess.workspace, commit=True, stream=st)
+        for s_ in range(sess.w.euler_steps):
+            ws.ws_fm_euler_step(sess.z[u], sess.vel[u][s_], 1.0 / sess.w.euler_steps, stream=st)
+
+    us = graph_time_us(step, reps, device)
+    return {"us_per_unit": round(us, 1), "value": round(sess.unit_flops(u) / (us * 1e-6) / 1e12, 3),
+            "unit": UNIT, "method": f"{reps} fused unit steps captured in one CUDA graph, replayed once"}
+
+
 def time_unit_graph(sess: UnitSession, device, reps: int = 50):
     """The whole unit step (append, attention, Euler steps) captured once in a
     CUDA graph and replayed: per-unit latency without host launch overhead."""
@@ -773,6 +794,7 @@ def main(argv=None):
             line["hbm_kernels"] = time_hbm_kernels(sess, device, peaks)
             line["graph"] = time_unit_graph(sess, device)
             line["attn_side"] = time_attn_side(sess, device, peaks)
+            line["graph_fused_commit"] = time_fused_unit(sess, device)
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(sess)
         print(json.dumps(line), flush=True)

@@ -134,6 +134,13 @@ WS_API ws_status ws_block_causal_attn(const void* q, const void* k_cache, const 
  *
  * k_side, v_side  device, [q_len][num_heads][head_dim] token-major (the same
  *                 layout as a slice for ws_kv_append), dtype dt
+ * commit          0: the cache is not written.  Nonzero: the kernel also
+ *                 writes the side K/V into cache rows [offsets[n_blocks-1],
+ *                 offsets[n_blocks]) of every head -- the same bytes
+ *                 ws_kv_append would write, from the tiles it has already
+ *                 loaded (the append fused into the attention); the solver's
+ *                 last step commits the clean slice this way.  Requires
+ *                 offsets[n_blocks] <= capacity.
  * The cache must hold blocks 0..n_blocks-2 (offsets[n_blocks-1] <= capacity,
  * else WS_ERR_CAPACITY); rows from offsets[n_blocks-1] on are not read.
  * Other arguments, the workspace (same size query) and errors as
@@ -141,7 +148,8 @@ WS_API ws_status ws_block_causal_attn(const void* q, const void* k_cache, const 
  * combinations return WS_ERR_UNSUPPORTED).
  */
 WS_API ws_status ws_block_causal_attn_side(const void* q, const void* k_cache, const void* v_cache,
-                                           const void* k_side, const void* v_side, void* out,
+                                           const void* k_side, const void* v_side, int commit,
+                                           void* out,
                                            float* lse_or_null, const int32_t* h_offsets,
                                            const int32_t* d_offsets, int n_blocks,
                                            int64_t capacity, int num_heads, int head_dim,

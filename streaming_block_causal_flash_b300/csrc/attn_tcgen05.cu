@@ -122,6 +122,10 @@ struct Params {
   // kv_tiles_c tiles; the newest block's n_side keys come from the
   // token-major side buffers, in the remaining kv_tiles - kv_tiles_c tiles.
   int side, kv_tiles_c, cache_len, n_side;
+  // Side mode with commit: the CTA holding query pair 0 of a group also
+  // stores every side tile it loads into cache rows cache_len + (row in the
+  // side buffer), through the store maps (extent cache_len + n_side rows).
+  int commit;
   long long work;
   int n_items;
   float scale_log2;
@@ -320,7 +324,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_ks,
-                    const __grid_constant__ CUtensorMap tm_vs, const Params P) {
+                    const __grid_constant__ CUtensorMap tm_vs,
+                    const __grid_constant__ CUtensorMap tm_kst,
+                    const __grid_constant__ CUtensorMap tm_vst, const Params P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -413,9 +419,24 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (from_side) {
               // side buffer [n_side][H*D]: 128 keys x 64 columns of head h
               const CUtensorMap* map = which == 0 ? &tm_ks : &tm_vs;
+              const uint32_t slot = sKV + ring.stage * TILE_BYTES;
               for (int hf = 0; hf < 2; ++hf)
-                tma_load_2d(sKV + ring.stage * TILE_BYTES + hf * HALF_BYTES, map, full,
-                            item.h * HD + hf * 64, kv0);
+                tma_load_2d(slot + hf * HALF_BYTES, map, full, item.h * HD + hf * 64, kv0);
+              if (P.commit && item.pair == 0) {
+                // commit the tile to the cache once it has landed, and keep the
+                // slot from being refilled until the store has read it
+                if (!wait_bar(full, ring.phase, abort_flag, P.timeout_ns, W_PROD_KVE)) {
+                  ok = false;
+                  ++issued;          // the loads are in flight: count them and
+                  ring.advance();    // move on, so the drain below waits for them
+                  break;
+                }
+                const CUtensorMap* dst = which == 0 ? &tm_kst : &tm_vst;
+                for (int hf = 0; hf < 2; ++hf)
+                  tma_store_3d(dst, slot + hf * HALF_BYTES, hf * 64, P.cache_len + kv0, item.h);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+              }
             } else {
               const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
               for (int hf = 0; hf < 2; ++hf)
@@ -442,6 +463,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (q_issued > 0)
         wait_bar(bar(BAR_Q_FULL), static_cast<uint32_t>(q_issued - 1) & 1u, &no_abort,
                  DRAIN_TIMEOUT_NS, W_DRAIN_TMA);
+      if (P.commit) bulk_wait_group0();   // committed tiles written before exit
     }
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
@@ -897,7 +919,8 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
-                                const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s) {
+                                const CUtensorMap& tm_vs, const CUtensorMap& tm_kst,
+                                const CUtensorMap& tm_vst, uint64_t timeout_ns, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -927,6 +950,7 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   P.kv_tiles_c = plan.kv_tiles_c;
   P.cache_len = plan.kv_len - plan.side_len;
   P.n_side = plan.side_len;
+  P.commit = (plan.side_len > 0 && a.commit) ? 1 : 0;
   P.groups = plan.groups;
   P.work = plan.work;
   P.n_items = plan.n_items;
@@ -940,7 +964,8 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   }
   P.timeout_ns = timeout_ns;
   P.force_stall = a.force_stall;
-  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs, P);
+  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs,
+                                                                  tm_kst, tm_vst, P);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (plan.split) {

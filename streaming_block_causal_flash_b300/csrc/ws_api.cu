@@ -90,7 +90,7 @@ ws_status check_attn_args(const char* who, const void* q, const void* k_cache,
                           const void* v_cache, void* out, const float* lse,
                           const int32_t* h_offsets, const int32_t* d_offsets, int n_blocks,
                           int64_t capacity, int num_heads, int head_dim, float softmax_scale,
-                          ws_dtype dt, bool side) {
+                          ws_dtype dt, bool side, bool commit) {
   if (!valid_dtype(dt)) return fail(WS_ERR_INVALID_ARGUMENT, "%s: unknown dtype %d", who, (int)dt);
   if (!q || !k_cache || !v_cache || !out || !h_offsets || !d_offsets)
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer argument", who);
@@ -106,7 +106,7 @@ ws_status check_attn_args(const char* who, const void* q, const void* k_cache,
       return fail(WS_ERR_INVALID_ARGUMENT, "%s: offsets decrease at block %d", who, b);
   // The cache holds every block read from it: all of them, or, when the
   // newest block comes from side buffers, the ones before it.
-  const int cached = side ? n_blocks - 1 : n_blocks;
+  const int cached = (side && !commit) ? n_blocks - 1 : n_blocks;
   if ((int64_t)h_offsets[cached] > capacity)
     return fail(WS_ERR_CAPACITY, "%s: offsets[%d]=%d exceeds capacity %lld", who, cached,
                 h_offsets[cached], (long long)capacity);
@@ -125,14 +125,15 @@ ws_status check_attn_args(const char* who, const void* q, const void* k_cache,
 }
 
 ws_status run_attention(const char* who, bool prefill, const void* q, const void* k_cache,
-                        const void* v_cache, const void* k_side, const void* v_side, void* out,
-                        float* lse, const int32_t* h_offsets,
+                        const void* v_cache, const void* k_side, const void* v_side, bool commit,
+                        void* out, float* lse, const int32_t* h_offsets,
                         const int32_t* d_offsets, int n_blocks, int64_t capacity, int num_heads,
                         int head_dim, float softmax_scale, ws_dtype dt, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
   const bool side = k_side != nullptr || v_side != nullptr;
   ws_status st = check_attn_args(who, q, k_cache, v_cache, out, lse, h_offsets, d_offsets,
-                                 n_blocks, capacity, num_heads, head_dim, softmax_scale, dt, side);
+                                 n_blocks, capacity, num_heads, head_dim, softmax_scale, dt, side,
+                                 side && commit);
   if (st != WS_OK) return st;
   if (side) {
     if (!k_side || !v_side)
@@ -188,7 +189,7 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   // views of the [H][capacity][D] caches, rows = the keys read from the cache
   // (kv_len, or q_row0 with side buffers), so rows beyond read as zeros; the
   // side buffers, like Q, as 2-D [q_len][H*D] matrices.
-  CUtensorMap tm_q, tm_k, tm_v, tm_ks, tm_vs;
+  CUtensorMap tm_q, tm_k, tm_v, tm_ks, tm_vs, tm_kst, tm_vst;
   const cuuint64_t D = (cuuint64_t)head_dim;
   {
     cuuint64_t dims[2] = {D * (cuuint64_t)num_heads, (cuuint64_t)q_len};
@@ -218,6 +219,19 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
     tm_ks = tm_k;    // unused without side buffers
     tm_vs = tm_v;
   }
+  if (side && commit) {
+    // store maps over the cache rows [0, kv_len): the side tiles land at rows
+    // q_row0 + (row in the side buffer); rows past kv_len are not written
+    cuuint64_t dims[3] = {D, (cuuint64_t)kv_len, (cuuint64_t)num_heads};
+    cuuint64_t strides[2] = {D * 2, (cuuint64_t)capacity * D * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    if (!encode_bf16(&tm_kst, k_cache, 3, dims, strides, box) ||
+        !encode_bf16(&tm_vst, v_cache, 3, dims, strides, box))
+      return fail(WS_ERR_CUDA, "%s: cannot encode the cache store maps", who);
+  } else {
+    tm_kst = tm_k;   // unused without a commit
+    tm_vst = tm_v;
+  }
   ws::TcAttnArgs a{};
   a.q = q;
   a.k_cache = k_cache;
@@ -229,7 +243,9 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   a.scale = scale;
   a.workspace = workspace;
   a.force_stall = g_force_stall;
-  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs, g_timeout_ns, stream);
+  a.commit = (side && commit) ? 1 : 0;
+  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs, tm_kst, tm_vst,
+                                          g_timeout_ns, stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
 }
@@ -306,7 +322,7 @@ ws_status ws_block_causal_attn(const void* q, const void* k_cache, const void* v
                                const int32_t* d_offsets, int n_blocks, int64_t capacity,
                                int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
                                void* workspace, size_t workspace_bytes, ws_stream_t stream) {
-  return run_attention("ws_block_causal_attn", false, q, k_cache, v_cache, nullptr, nullptr, out,
+  return run_attention("ws_block_causal_attn", false, q, k_cache, v_cache, nullptr, nullptr, false, out,
                        lse_or_null,
                        h_offsets, d_offsets, n_blocks, capacity, num_heads, head_dim,
                        softmax_scale, dt, workspace, workspace_bytes, stream);
@@ -317,14 +333,14 @@ ws_status ws_block_causal_prefill(const void* q, const void* k_cache, const void
                                   const int32_t* d_offsets, int n_blocks, int64_t capacity,
                                   int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
                                   void* workspace, size_t workspace_bytes, ws_stream_t stream) {
-  return run_attention("ws_block_causal_prefill", true, q, k_cache, v_cache, nullptr, nullptr, out,
+  return run_attention("ws_block_causal_prefill", true, q, k_cache, v_cache, nullptr, nullptr, false, out,
                        lse_or_null,
                        h_offsets, d_offsets, n_blocks, capacity, num_heads, head_dim,
                        softmax_scale, dt, workspace, workspace_bytes, stream);
 }
 
 ws_status ws_block_causal_attn_side(const void* q, const void* k_cache, const void* v_cache,
-                                    const void* k_side, const void* v_side, void* out,
+                                    const void* k_side, const void* v_side, int commit, void* out,
                                     float* lse_or_null, const int32_t* h_offsets,
                                     const int32_t* d_offsets, int n_blocks, int64_t capacity,
                                     int num_heads, int head_dim, float softmax_scale, ws_dtype dt,
@@ -332,7 +348,7 @@ ws_status ws_block_causal_attn_side(const void* q, const void* k_cache, const vo
   const char* who = "ws_block_causal_attn_side";
   if (!k_side || !v_side)
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: k_side and v_side are required", who);
-  return run_attention(who, false, q, k_cache, v_cache, k_side, v_side, out, lse_or_null,
+  return run_attention(who, false, q, k_cache, v_cache, k_side, v_side, commit != 0, out, lse_or_null,
                        h_offsets, d_offsets, n_blocks, capacity, num_heads, head_dim,
                        softmax_scale, dt, workspace, workspace_bytes, stream);
 }

@@ -39,8 +39,8 @@ SIGNATURES = {
                                       _c_int, _c_f32, _c_int, _vp, _c_size, _vp]),
     "ws_block_causal_prefill": (_c_int, [_vp, _vp, _vp, _vp, _vp, _i32p, _vp, _c_int, _c_i64, _c_int,
                                          _c_int, _c_f32, _c_int, _vp, _c_size, _vp]),
-    "ws_block_causal_attn_side": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32p, _vp, _c_int, _c_i64,
-                                           _c_int, _c_int, _c_f32, _c_int, _vp, _c_size, _vp]),
+    "ws_block_causal_attn_side": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _i32p, _vp, _c_int,
+                                           _c_i64, _c_int, _c_int, _c_f32, _c_int, _vp, _c_size, _vp]),
     "ws_block_causal_attn_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _i32p, _vp, _c_int, _c_i64,
                                               _c_int, _c_int, _c_f32, _c_int, _vp]),
     "ws_fm_euler_step": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _c_i64, _c_f32, _vp]),
@@ -175,9 +175,12 @@ def ws_block_causal_attn(q, k_cache, v_cache, out, offsets_host: Sequence[int],
 def ws_block_causal_attn_side(q, k_cache, v_cache, k_side, v_side, out,
                               offsets_host: Sequence[int], offsets_dev: torch.Tensor,
                               lse: Optional[torch.Tensor] = None, softmax_scale: float = 0.0,
-                              workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+                              workspace: Optional[torch.Tensor] = None, commit: bool = False,
+                              stream=None) -> None:
     """Newest unit's queries against the cache (blocks before the last) plus
-    the unit's own K/V from token-major side buffers [q_len, H, D]."""
+    the unit's own K/V from token-major side buffers [q_len, H, D]; with
+    commit=True the kernel also writes those K/V into the cache rows of the
+    last block (the append fused into the attention)."""
     H, cap, D = k_cache.shape
     dt = q.dtype
     offs = _host_offsets(offsets_host)
@@ -194,7 +197,7 @@ def ws_block_causal_attn_side(q, k_cache, v_cache, k_side, v_side, out,
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     _check(load().ws_block_causal_attn_side(
         _dev(q, "q"), _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
-        _dev(k_side, "k_side", dt), _dev(v_side, "v_side", dt), _dev(out, "out", dt),
+        _dev(k_side, "k_side", dt), _dev(v_side, "v_side", dt), 1 if commit else 0, _dev(out, "out", dt),
         _dev(lse, "lse", torch.float32), offs.ctypes.data_as(_i32p),
         _dev(offsets_dev, "offsets_dev", torch.int32), int(offs.size - 1), int(cap), int(H), int(D),
         float(softmax_scale), _dtype_code(q), ws_ptr, ws_bytes, _stream_ptr(stream)))

@@ -90,15 +90,16 @@ def test_attention_host_validation(lib, fn):
 def test_side_attention_host_validation(lib):
     f = lib.ws_block_causal_attn_side
 
-    def call(offs_vals, ks=FAKE, vs=FAKE, dt=ws.WS_BF16, cap=1024, D=128):
+    def call(offs_vals, ks=FAKE, vs=FAKE, dt=ws.WS_BF16, cap=1024, D=128, commit=0):
         arr, p = _offs(offs_vals)
-        return f(FAKE, FAKE, FAKE, ks, vs, FAKE, None, p, FAKE, len(arr) - 1, cap, 2, D, 0.0, dt,
-                 None, 0, None)
+        return f(FAKE, FAKE, FAKE, ks, vs, commit, FAKE, None, p, FAKE, len(arr) - 1, cap, 2, D, 0.0,
+                 dt, None, 0, None)
     assert call([0, 8, 16], ks=0) == ws.WS_ERR_INVALID_ARGUMENT          # missing side buffer
     assert call([0, 8, 16], vs=FAKE + 8) == ws.WS_ERR_INVALID_ARGUMENT   # misaligned side buffer
     assert call([0, 8, 16], dt=ws.WS_F32) == ws.WS_ERR_UNSUPPORTED        # bf16 only
     assert call([0, 1100, 1200]) == ws.WS_ERR_CAPACITY                   # history past capacity
     assert call([0, 9, 5]) == ws.WS_ERR_INVALID_ARGUMENT                 # decreasing offsets
+    assert call([0, 1000, 1100], commit=1) == ws.WS_ERR_CAPACITY          # commit needs room for the unit
 
 
 def test_euler_host_validation(lib):

@@ -132,3 +132,77 @@ def test_side_unit_640x368_sampled_rows():
                          k_side[:, heads].float().cpu().numpy(), v_side[:, heads].float().cpu().numpy(), lo)
     ref, _ = bc.attention_rows(sess.q_host[u][rows][:, heads].float().numpy(), lo + rows, k, v, offs)
     assert_close_bf16(out[rows][:, heads].float().cpu().numpy(), ref, "640x368 side")
+
+
+# ------------------------------------------------- fused commit (append fused in)
+
+@pytest.mark.parametrize("seed,heads,sizes", [
+    (51, 2, [300, 77]),
+    (52, 3, [1000, 1000, 600]),
+    (53, 1, [40]),                  # no history
+    (54, 2, [8000, 300]),           # split key range: several groups share the head
+    (55, 4, [0, 130, 0, 260]),
+    (56, 1, [129, 127, 256, 1, 255]),
+])
+def test_side_commit_writes_the_slice_and_nothing_else(seed, heads, sizes):
+    case = side_case(seed, heads, sizes, cap_extra=37)
+    lo, hi = int(case.offsets[-2]), int(case.offsets[-1])
+    case.k[:, hi:] = 7.0            # canary rows past the unit
+    case.v[:, hi:] = -3.0
+    k_before, v_before = case.k.clone(), case.v.clone()
+    H, q_len = heads, case.q.shape[0]
+    out = torch.full_like(case.q, float("nan"))
+    wsp = ws.workspace_for(q_len, case.T, H, 128)
+    ws.ws_block_causal_attn_side(case.q, case.k, case.v, case.k_side, case.v_side, out, case.offsets,
+                                 case.offs_dev, workspace=wsp, commit=True)
+    torch.cuda.synchronize()
+    # the unit's rows hold the slice, bit for bit; every other row is as before
+    assert torch.equal(case.k[:, lo:hi], case.k_side.transpose(0, 1))
+    assert torch.equal(case.v[:, lo:hi], case.v_side.transpose(0, 1))
+    for t, before in ((case.k, k_before), (case.v, v_before)):
+        assert torch.equal(t[:, :lo], before[:, :lo])
+        assert torch.equal(t[:, hi:], before[:, hi:])
+    ref, _ = oracle_with_side(case, case.k_side, case.v_side)
+    assert_close_bf16(out.float().cpu().numpy(), ref, f"side+commit {sizes}")
+
+
+def test_solver_steps_then_fused_commit():
+    """Three noisy steps through side buffers, the last one commits its slice
+    in the same call; the plain attention over the cache then agrees."""
+    case = side_case(57, 2, [3000, 2000, 934])
+    n = case.q.shape[0]
+    lo, hi = int(case.offsets[-2]), int(case.offsets[-1])
+    wsp = ws.workspace_for(n, case.T, 2, 128)
+    for step in range(3):
+        ks = normal(57, "k_noisy", step, (n, 2, 128), 0.5, torch.bfloat16).cuda()
+        vs = normal(57, "v_noisy", step, (n, 2, 128), 0.5, torch.bfloat16).cuda()
+        out = torch.empty_like(case.q)
+        ws.ws_block_causal_attn_side(case.q, case.k, case.v, ks, vs, out, case.offsets, case.offs_dev,
+                                     workspace=wsp, commit=(step == 2))
+    torch.cuda.synchronize()
+    assert torch.equal(case.k[:, lo:hi], ks.transpose(0, 1))
+    plain = torch.empty_like(case.q)
+    ws.ws_block_causal_attn(case.q, case.k, case.v, plain, case.offsets, case.offs_dev, workspace=wsp)
+    torch.cuda.synchronize()
+    ref, _ = oracle_with_side(case, ks, vs)
+    assert_close_bf16(out.float().cpu().numpy(), ref, "last side step")
+    assert_close_bf16(plain.float().cpu().numpy(), ref, "after fused commit")
+
+
+def test_side_commit_unit_640x368_matches_append():
+    """At full size the fused commit writes exactly what ws_kv_append writes."""
+    w = WORKLOADS["unit_640x368"]
+    sess = bench.UnitSession(w, torch.device("cuda"))
+    u = sess.units[0]
+    n = sess.sizes[u]
+    offs = sess.offsets_all[:u + 2]
+    lo = int(offs[-2])
+    k_side, v_side = sess.kv[u]
+    k_ref, v_ref = sess.k.clone(), sess.v.clone()
+    ws.ws_kv_append(k_side, v_side, k_ref, v_ref, lo)
+    out = torch.empty(n, w.heads, w.head_dim, dtype=torch.bfloat16, device="cuda")
+    ws.ws_block_causal_attn_side(sess.q[u], sess.k, sess.v, k_side, v_side, out, offs,
+                                 sess.offs_dev[u], workspace=sess.workspace, commit=True)
+    torch.cuda.synchronize()
+    assert torch.equal(sess.k, k_ref)
+    assert torch.equal(sess.v, v_ref)
