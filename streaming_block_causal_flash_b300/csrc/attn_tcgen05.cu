@@ -17,8 +17,9 @@
 //   warp  9    TMEM owner; its lane 0 issues every MMA of query tile 0
 //   warp  10   lane 0 issues every MMA of query tile 1 (two issuers keep the
 //              tensor pipe fed while the other one waits on barriers)
-//   warp  11   idle (it completes the third warpgroup, which gives up
-//              registers to the softmax warpgroups)
+//   warp  11   side mode with commit: lane 0 stores the newest unit's K/V
+//              tiles into the cache (otherwise idle; it completes the third
+//              warpgroup, which gives up registers to the softmax warpgroups)
 // TMEM (512 columns): tile t uses S_t = cols [256t, 256t+128) (fp32 logits,
 // overwritten in place by bf16 P in its first 64 columns) and
 // O_t = cols [256t+128, 256t+256) (fp32 output accumulator).
@@ -345,7 +346,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), 1);
-      mbar_init(bar(BAR_KV_EMPTY + s), 2);      // released by both MMA issuers
+      // released by both MMA issuers (and, with commit, the store warp)
+      mbar_init(bar(BAR_KV_EMPTY + s), 2 + P.commit);
     }
     mbar_init(bar(BAR_Q_FULL), 1);
     mbar_init(bar(BAR_Q_EMPTY), 2);
@@ -419,24 +421,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (from_side) {
               // side buffer [n_side][H*D]: 128 keys x 64 columns of head h
               const CUtensorMap* map = which == 0 ? &tm_ks : &tm_vs;
-              const uint32_t slot = sKV + ring.stage * TILE_BYTES;
               for (int hf = 0; hf < 2; ++hf)
-                tma_load_2d(slot + hf * HALF_BYTES, map, full, item.h * HD + hf * 64, kv0);
-              if (P.commit && item.pair == 0) {
-                // commit the tile to the cache once it has landed, and keep the
-                // slot from being refilled until the store has read it
-                if (!wait_bar(full, ring.phase, abort_flag, P.timeout_ns, W_PROD_KVE)) {
-                  ok = false;
-                  ++issued;          // the loads are in flight: count them and
-                  ring.advance();    // move on, so the drain below waits for them
-                  break;
-                }
-                const CUtensorMap* dst = which == 0 ? &tm_kst : &tm_vst;
-                for (int hf = 0; hf < 2; ++hf)
-                  tma_store_3d(dst, slot + hf * HALF_BYTES, hf * 64, P.cache_len + kv0, item.h);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-              }
+                tma_load_2d(sKV + ring.stage * TILE_BYTES + hf * HALF_BYTES, map, full,
+                            item.h * HD + hf * 64, kv0);
             } else {
               const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
               for (int hf = 0; hf < 2; ++hf)
@@ -463,7 +450,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (q_issued > 0)
         wait_bar(bar(BAR_Q_FULL), static_cast<uint32_t>(q_issued - 1) & 1u, &no_abort,
                  DRAIN_TIMEOUT_NS, W_DRAIN_TMA);
-      if (P.commit) bulk_wait_group0();   // committed tiles written before exit
     }
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
@@ -577,6 +563,57 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mma_commit(bar(BAR_DRAIN + t));
       volatile int no_abort = 0;
       wait_bar(bar(BAR_DRAIN + t), 0u, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_MMA);
+    }
+    __syncwarp();
+  } else if (warp == 11 && P.commit) {
+    // -------------------------------------- store warp (side mode, commit)
+    // A third consumer of the K/V ring: it waits for every slot to fill.
+    // Side tile js of a head is stored by the group's CTA with query pair
+    // js % pairs (each tile exactly once, the work spread over the group),
+    // into cache rows cache_len + (side row); rows past kv_len are clipped
+    // by the store maps.  A stored slot is released one slot use later,
+    // once its store has read it, so the read overlaps the next wait.
+    if (lane == 0) {
+      ItemIter it;
+      iter_init(P, it);
+      Item item;
+      Ring ring;
+      bool ok = true;
+      int held = -1;     // slot whose store may still be reading it
+      while (ok && iter_next(P, it, item)) {
+        const int n_iter = max(item.n[0], item.n[1]);
+        for (int j = 0; j < n_iter && ok; ++j) {
+          const int tile = item.t0 + j;
+          const int js = tile - P.kv_tiles_c;
+          const bool store = js >= 0 && js % P.pairs == item.pair;
+          for (int which = 0; which < 2; ++which) {
+            const int stage = static_cast<int>(ring.stage);
+            const uint32_t slot = sKV + ring.stage * TILE_BYTES;
+            if (!wait_bar(bar(BAR_KV_FULL + ring.stage), ring.phase, abort_flag, P.timeout_ns,
+                          W_MMA_KV)) { ok = false; break; }
+            if (store) {
+              const CUtensorMap* dst = which == 0 ? &tm_kst : &tm_vst;
+              for (int hf = 0; hf < 2; ++hf)
+                tma_store_3d(dst, slot + hf * HALF_BYTES, hf * 64, P.cache_len + js * BN, item.h);
+              bulk_commit_group();
+            }
+            if (held >= 0) {
+              if (store) bulk_wait_group_read1();   // all but the store just issued
+              else bulk_wait_group_read0();
+              mbar_arrive(bar(BAR_KV_EMPTY + held));
+              held = -1;
+            }
+            if (store) held = stage;
+            else mbar_arrive(bar(BAR_KV_EMPTY + ring.stage));
+            ring.advance();
+          }
+        }
+      }
+      if (held >= 0) {
+        bulk_wait_group_read0();
+        mbar_arrive(bar(BAR_KV_EMPTY + held));
+      }
+      bulk_wait_group0();   // every committed tile written before the CTA exits
     }
     __syncwarp();
   }
