@@ -102,6 +102,22 @@ def test_side_attention_host_validation(lib):
     assert call([0, 1000, 1100], commit=1) == ws.WS_ERR_CAPACITY          # commit needs room for the unit
 
 
+def test_empty_query_block_is_a_no_op(lib):
+    """An empty newest block (equal last offsets) or an empty sequence has no
+    query rows: every attention call returns WS_OK before touching memory
+    (the pointers here are never dereferenced)."""
+    for offs_vals in ([0, 8, 8], [0, 0], [0, 0, 0]):
+        arr, p = _offs(offs_vals)
+        for fn in ("ws_block_causal_attn", "ws_block_causal_prefill"):
+            if fn == "ws_block_causal_prefill" and offs_vals[-1] != 0:
+                continue                      # the prefill has rows there
+            assert getattr(lib, fn)(FAKE, FAKE, FAKE, FAKE, None, p, FAKE, len(arr) - 1, 64, 2, 128,
+                                    0.0, ws.WS_BF16, None, 0, None) == ws.WS_OK
+        assert lib.ws_block_causal_attn_side(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, None, p, FAKE,
+                                             len(arr) - 1, 64, 2, 128, 0.0, ws.WS_BF16, None, 0,
+                                             None) == ws.WS_OK
+
+
 def test_euler_host_validation(lib):
     assert lib.ws_fm_euler_step(FAKE, ws.WS_BF16, FAKE, ws.WS_BF16, None, 8, 0.25, None) == ws.WS_ERR_UNSUPPORTED
     assert lib.ws_fm_euler_step(FAKE, ws.WS_F32, FAKE + 4, ws.WS_BF16, None, 8, 0.25, None) == \
