@@ -150,8 +150,15 @@ class ClockSampler:
 
 
 def source_digest(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] of the kernel source's code: // comments, blank lines and
+    trailing spaces removed, so that a comment edit keeps recorded counters."""
+    code = []
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            line = line.split("//", 1)[0].rstrip()
+            if line:
+                code.append(line)
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
 def recorded_traffic(workload: str = DEFAULT_WORKLOAD):

@@ -24,14 +24,15 @@
 // overwritten in place by bf16 P in its first 64 columns) and
 // O_t = cols [256t+128, 256t+256) (fp32 output accumulator).
 //
-// Per key tile j, the issuer of query tile t issues PV_t(j-1) then QK_t(j);
-// the two issuers run independently, so while one softmax group works on
-// S_t(j) the tensor pipe executes the other tile's PV and QK.  tcgen05.mma
-// instructions from one thread execute in issue order, which orders QK_t(j)
-// (writes S_t) after PV_t(j-1) (reads P_t from the same columns).  One
-// thread issuing both tiles' MMAs left the pipe idle during its barrier
-// waits and fences (about 115 cycles per 64-cycle MMA); two issuers hide
-// that bookkeeping behind each other's MMAs.
+// Per key tile j, the issuer of query tile t waits for K_j, then for P_t(j-1),
+// and issues PV_t(j-1) then QK_t(j) as one group under a shared-memory issue
+// lock, so the two tiles' groups reach the tensor pipe whole; while one
+// softmax group works on S_t(j) the pipe executes the other tile's group.
+// tcgen05.mma instructions from one thread execute in issue order, which
+// orders QK_t(j) (writes S_t) after PV_t(j-1) (reads P_t from the same
+// columns).  One thread issuing both tiles' MMAs left the pipe idle during
+// its barrier waits and fences (about 115 cycles per 64-cycle MMA); two
+// issuers hide that bookkeeping behind each other's MMAs.
 //
 // Softmax keeps a per-row running max m (log2 units of the scaled logits) and
 // sum l.  O is rescaled only when a row's max grows by more than 2^8 (lazy
@@ -49,6 +50,10 @@
 //    nearly the same time (one HBM read, L2 reuse).  A range that covers only
 //    part of a head writes a partial (O/l, log2-sum-exp) into the workspace;
 //    attn_combine_kernel merges the partials.
+//    Side mode (unit mode only): keys [0, cache_len) come from the cache and
+//    the newest unit's keys from token-major side buffers through 2-D TMA
+//    maps; the two parts are tiled separately, each with its own ragged tail.
+//    With commit, warp 11 also stores the side tiles into the cache.
 //  * prefill mode: one work item per (head, query-tile pair), head-major,
 //    longest key range first; key tiles no row of a query tile can see are
 //    skipped; CTAs take items round-robin.
