@@ -66,3 +66,28 @@ def test_clock_sampler_without_nvidia_smi(monkeypatch):
     s = bench.ClockSampler(0)
     s.start()
     assert s.stop()["samples"] == 0
+
+
+def test_reference_arm_under_torchrun_two_ranks(tmp_path):
+    """bench.py --impl reference launched like the multi-GPU arm (torchrun,
+    two ranks, gloo on CPU): rank 0 prints exactly one JSON line for the
+    oracle, the other rank exits 0 without output."""
+    import json
+    import socket
+    import subprocess
+    import sys
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(root, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+           "--workload", "unit_192x336"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
