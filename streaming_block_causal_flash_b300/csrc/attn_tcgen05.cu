@@ -17,8 +17,8 @@
 //   warp  9    TMEM owner; its lane 0 issues every MMA of query tile 0
 //   warp  10   lane 0 issues every MMA of query tile 1 (two issuers keep the
 //              tensor pipe fed while the other one waits on barriers)
-//   warp  11   side mode with commit: lane 0 stores the newest unit's K/V
-//              tiles into the cache (otherwise idle; it completes the third
+//   warp  11   side mode with commit: copies the newest unit's K/V tiles
+//              into the cache (otherwise idle; it completes the third
 //              warpgroup, which gives up registers to the softmax warpgroups)
 // TMEM (512 columns): tile t uses S_t = cols [256t, 256t+128) (fp32 logits,
 // overwritten in place by bf16 P in its first 64 columns) and
@@ -53,7 +53,7 @@
 //    Side mode (unit mode only): keys [0, cache_len) come from the cache and
 //    the newest unit's keys from token-major side buffers through 2-D TMA
 //    maps; the two parts are tiled separately, each with its own ragged tail.
-//    With commit, warp 11 also stores the side tiles into the cache.
+//    With commit, warp 11 also copies the side tiles into the cache.
 //  * prefill mode: one work item per (head, query-tile pair), head-major,
 //    longest key range first; key tiles no row of a query tile can see are
 //    skipped; CTAs take items round-robin.
@@ -128,10 +128,13 @@ struct Params {
   // kv_tiles_c tiles; the newest block's n_side keys come from the
   // token-major side buffers, in the remaining kv_tiles - kv_tiles_c tiles.
   int side, kv_tiles_c, cache_len, n_side;
-  // Side mode with commit: the CTA holding query pair 0 of a group also
-  // stores every side tile it loads into cache rows cache_len + (row in the
-  // side buffer), through the store maps (extent cache_len + n_side rows).
+  // Side mode with commit: the store warp copies the side tiles it owns into
+  // cache rows cache_len + (row in the side buffer) of k_cache / v_cache
+  // ([H][capacity][HD]).
   int commit;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  long long capacity;
   long long work;
   int n_items;
   float scale_log2;
@@ -330,9 +333,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_ks,
-                    const __grid_constant__ CUtensorMap tm_vs,
-                    const __grid_constant__ CUtensorMap tm_kst,
-                    const __grid_constant__ CUtensorMap tm_vst, const Params P) {
+                    const __grid_constant__ CUtensorMap tm_vs, const Params P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -573,18 +574,19 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   } else if (warp == 11 && P.commit) {
     // -------------------------------------- store warp (side mode, commit)
     // A third consumer of the K/V ring: it waits for every slot to fill.
-    // Side tile js of a head is stored by the group's CTA with query pair
-    // js % pairs (each tile exactly once, the work spread over the group),
-    // into cache rows cache_len + (side row); rows past kv_len are clipped
-    // by the store maps.  A stored slot is released one slot use later,
-    // once its store has read it, so the read overlaps the next wait.
-    if (lane == 0) {
+    // Side tile js of a head is copied by the group's CTA with query pair
+    // js % pairs (each tile exactly once, the work spread over the group):
+    // all 32 lanes read the 128-byte-swizzled tile from shared memory in
+    // 16-byte chunks and write them to cache rows cache_len + (side row),
+    // skipping rows past the unit.  Plain loads and stores keep the TMA unit
+    // free for the ring's loads (TMA stores measured twice as costly).  The
+    // slot is released once the copy has read it.
+    {
       ItemIter it;
       iter_init(P, it);
       Item item;
       Ring ring;
       bool ok = true;
-      int held = -1;     // slot whose store may still be reading it
       while (ok && iter_next(P, it, item)) {
         const int n_iter = max(item.n[0], item.n[1]);
         for (int j = 0; j < n_iter && ok; ++j) {
@@ -592,33 +594,35 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           const int js = tile - P.kv_tiles_c;
           const bool store = js >= 0 && js % P.pairs == item.pair;
           for (int which = 0; which < 2; ++which) {
-            const int stage = static_cast<int>(ring.stage);
-            const uint32_t slot = sKV + ring.stage * TILE_BYTES;
-            if (!wait_bar(bar(BAR_KV_FULL + ring.stage), ring.phase, abort_flag, P.timeout_ns,
-                          W_MMA_KV)) { ok = false; break; }
+            const uint32_t full = bar(BAR_KV_FULL + ring.stage);
+            int got = 1;
+            if (lane == 0) got = wait_bar(full, ring.phase, abort_flag, P.timeout_ns, W_MMA_KV);
+            if (__shfl_sync(0xffffffffu, got, 0) == 0) { ok = false; break; }
+            // every lane observes the completed phase, which makes the
+            // tile's TMA writes visible to it (returns at once)
+            for (int w = 0; w < 1000000 && !mbar_try_wait(full, ring.phase); ++w) {}
             if (store) {
-              const CUtensorMap* dst = which == 0 ? &tm_kst : &tm_vst;
-              for (int hf = 0; hf < 2; ++hf)
-                tma_store_3d(dst, slot + hf * HALF_BYTES, hf * 64, P.cache_len + js * BN, item.h);
-              bulk_commit_group();
+              const uint8_t* src = sgen + SMEM_KV + ring.stage * TILE_BYTES;
+              __nv_bfloat16* cache = which == 0 ? P.k_cache : P.v_cache;
+              const int rows = min(BN, P.n_side - js * BN);
+              const size_t row0 = static_cast<size_t>(item.h) * P.capacity + P.cache_len + js * BN;
+              for (int i = lane; i < 2 * BN * 8; i += 32) {
+                const int hf = i / (BN * 8);          // 64-column half
+                const int r = (i >> 3) % BN;          // key row in the tile
+                const int c = i & 7;                  // 16-byte chunk in the half-row
+                if (r < rows) {
+                  const uint4 v = *reinterpret_cast<const uint4*>(
+                      src + hf * HALF_BYTES + r * 128 + ((c ^ (r & 7)) << 4));
+                  *reinterpret_cast<uint4*>(cache + (row0 + r) * HD + hf * 64 + c * 8) = v;
+                }
+              }
             }
-            if (held >= 0) {
-              if (store) bulk_wait_group_read1();   // all but the store just issued
-              else bulk_wait_group_read0();
-              mbar_arrive(bar(BAR_KV_EMPTY + held));
-              held = -1;
-            }
-            if (store) held = stage;
-            else mbar_arrive(bar(BAR_KV_EMPTY + ring.stage));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_KV_EMPTY + ring.stage));
             ring.advance();
           }
         }
       }
-      if (held >= 0) {
-        bulk_wait_group_read0();
-        mbar_arrive(bar(BAR_KV_EMPTY + held));
-      }
-      bulk_wait_group0();   // every committed tile written before the CTA exits
     }
     __syncwarp();
   }
@@ -961,8 +965,7 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
-                                const CUtensorMap& tm_vs, const CUtensorMap& tm_kst,
-                                const CUtensorMap& tm_vst, uint64_t timeout_ns, cudaStream_t s) {
+                                const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -993,6 +996,9 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   P.cache_len = plan.kv_len - plan.side_len;
   P.n_side = plan.side_len;
   P.commit = (plan.side_len > 0 && a.commit) ? 1 : 0;
+  P.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.k_cache));
+  P.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.v_cache));
+  P.capacity = a.capacity;
   P.groups = plan.groups;
   P.work = plan.work;
   P.n_items = plan.n_items;
@@ -1006,8 +1012,7 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   }
   P.timeout_ns = timeout_ns;
   P.force_stall = a.force_stall;
-  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs,
-                                                                  tm_kst, tm_vst, P);
+  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs, P);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (plan.split) {

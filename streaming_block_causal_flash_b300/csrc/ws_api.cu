@@ -189,7 +189,7 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   // views of the [H][capacity][D] caches, rows = the keys read from the cache
   // (kv_len, or q_row0 with side buffers), so rows beyond read as zeros; the
   // side buffers, like Q, as 2-D [q_len][H*D] matrices.
-  CUtensorMap tm_q, tm_k, tm_v, tm_ks, tm_vs, tm_kst, tm_vst;
+  CUtensorMap tm_q, tm_k, tm_v, tm_ks, tm_vs;
   const cuuint64_t D = (cuuint64_t)head_dim;
   {
     cuuint64_t dims[2] = {D * (cuuint64_t)num_heads, (cuuint64_t)q_len};
@@ -219,19 +219,6 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
     tm_ks = tm_k;    // unused without side buffers
     tm_vs = tm_v;
   }
-  if (side && commit) {
-    // store maps over the cache rows [0, kv_len): the side tiles land at rows
-    // q_row0 + (row in the side buffer); rows past kv_len are not written
-    cuuint64_t dims[3] = {D, (cuuint64_t)kv_len, (cuuint64_t)num_heads};
-    cuuint64_t strides[2] = {D * 2, (cuuint64_t)capacity * D * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    if (!encode_bf16(&tm_kst, k_cache, 3, dims, strides, box) ||
-        !encode_bf16(&tm_vst, v_cache, 3, dims, strides, box))
-      return fail(WS_ERR_CUDA, "%s: cannot encode the cache store maps", who);
-  } else {
-    tm_kst = tm_k;   // unused without a commit
-    tm_vst = tm_v;
-  }
   ws::TcAttnArgs a{};
   a.q = q;
   a.k_cache = k_cache;
@@ -244,8 +231,8 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   a.workspace = workspace;
   a.force_stall = g_force_stall;
   a.commit = (side && commit) ? 1 : 0;
-  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs, tm_kst, tm_vst,
-                                          g_timeout_ns, stream);
+  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs, g_timeout_ns,
+                                          stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
 }

@@ -84,8 +84,7 @@ struct TcAttnArgs {
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
-                                const CUtensorMap& tm_vs, const CUtensorMap& tm_kst,
-                                const CUtensorMap& tm_vst, uint64_t timeout_ns, cudaStream_t s);
+                                const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s);
 cudaError_t read_attn_device_error(int* code, int* info);
 cudaError_t clear_attn_device_error();
 
