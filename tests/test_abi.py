@@ -147,3 +147,62 @@ def test_binding_raises_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ws, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         ws.load()
+
+
+def _header_params():
+    """{function name: parameter count} from the WS_API declarations."""
+    text = open(os.path.join(ROOT, "include", "ws.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"WS_API\s+[\w\s\*]+?\b(ws_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [p for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        out[m.group(1)] = len(params)
+    return out
+
+
+def test_binding_argument_counts_match_the_header():
+    params = _header_params()
+    assert set(params) == set(ws.SIGNATURES)
+    for name, (_, argtypes) in ws.SIGNATURES.items():
+        assert len(argtypes) == params[name], name
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """A C99 translation unit that includes ws.h and calls every entry point
+    compiles without warnings and links against the built library (it is not
+    run: no GPU is needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_ws.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "ws.h"
+int main(void) {
+  int32_t offs[3] = {0, 8, 16};
+  int code = 0, info = 0;
+  ws_stream_t s = NULL;
+  ws_status st = ws_kv_append(NULL, NULL, NULL, NULL, 0, 0, 16, 1, 128, WS_BF16, s);
+  st |= ws_block_causal_attn(NULL, NULL, NULL, NULL, NULL, offs, NULL, 2, 16, 1, 128, 0.f, WS_BF16, NULL, 0, s);
+  st |= ws_block_causal_attn_side(NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL, offs, NULL, 2, 16, 1, 128, 0.f,
+                                  WS_BF16, NULL, 0, s);
+  st |= ws_block_causal_attn_noalloc(NULL, NULL, NULL, NULL, NULL, offs, NULL, 2, 16, 1, 128, 0.f, WS_BF16, s);
+  st |= ws_block_causal_prefill(NULL, NULL, NULL, NULL, NULL, offs, NULL, 2, 16, 1, 128, 0.f, WS_BF16, NULL, 0, s);
+  st |= ws_fm_euler_step(NULL, WS_F32, NULL, WS_BF16, NULL, 0, 0.25f, s);
+  st |= ws_fm_euler_cfg_step(NULL, WS_F32, NULL, NULL, WS_BF16, NULL, 0, 2.f, 0.25f, s);
+  size_t n = ws_block_causal_attn_workspace_size(8, 16, 1, 128);
+  st |= ws_get_device_error(&code, &info);
+  st |= ws_clear_device_error();
+  st |= ws_set_wait_timeout_ns(1000000000ull);
+  st |= ws_debug_force_wait_timeout(0);
+  printf("%s %s %zu %d\n", ws_status_string(st), ws_last_error(), n, ws_abi_version());
+  return 0;
+}
+''')
+    lib_dir = os.path.dirname(ws_build.LIB_PATH)
+    res = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                          str(src), "-L", lib_dir, "-l:" + os.path.basename(ws_build.LIB_PATH),
+                          "-o", str(tmp_path / "use_ws")], capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
