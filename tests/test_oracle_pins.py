@@ -116,6 +116,40 @@ def test_attention_matches_bruteforce_mask(seed):
         np.testing.assert_allclose(lse[h], scipy.special.logsumexp(x, axis=1), rtol=1e-12, atol=1e-12)
 
 
+from hypothesis import given, settings, strategies as st
+
+
+@settings(max_examples=60, deadline=None, derandomize=True)
+@given(sizes=st.lists(st.integers(0, 9), min_size=1, max_size=8),
+       heads=st.integers(1, 3), head_dim=st.sampled_from([1, 4, 8]),
+       scale=st.floats(0.05, 2.0), seed=st.integers(0, 2 ** 16))
+def test_attention_matches_scipy_softmax_for_random_layouts(sizes, heads, head_dim, scale, seed):
+    """Random block layouts (empty blocks included): every row of the oracle
+    equals scipy's softmax over the keys of its own and earlier blocks, with
+    the block of each token found by walking the sizes; the unit call on the
+    last block gives the same rows as the full sequence."""
+    if sum(sizes) == 0:
+        sizes = sizes + [1]
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    T = int(offsets[-1])
+    rng = _rng(seed)
+    q, k, v = _qkv(rng, T, heads, head_dim)
+    out, lse = bc.block_causal_attention(q, k, v, offsets, scale)
+    ids = _block_ids_by_scan(offsets)
+    for i in range(T):
+        vis = ids <= ids[i]
+        for h in range(heads):
+            x = scale * (k[h][vis] @ q[i, h])
+            w = scipy.special.softmax(x)
+            np.testing.assert_allclose(out[i, h], w @ v[h][vis], rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(lse[h, i], scipy.special.logsumexp(x), rtol=1e-12, atol=1e-12)
+    lo = int(offsets[-2])
+    if T > lo:
+        out_u, lse_u = bc.unit_attention(q[lo:], k, v, offsets, scale)
+        np.testing.assert_array_equal(out_u, out[lo:])
+        np.testing.assert_array_equal(lse_u, lse[:, lo:])
+
+
 def test_one_block_is_full_attention_sdpa():
     rng = _rng(7)
     T, H, D = 37, 4, 16
