@@ -283,8 +283,8 @@ ws_status ws_kv_append(const void* k_new, const void* v_new, void* k_cache, void
   if (!valid_dtype(dt)) return fail(WS_ERR_INVALID_ARGUMENT, "%s: unknown dtype", who);
   if (n_new < 0 || cache_len < 0 || capacity < 0 || num_heads < 1 || head_dim < 1)
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: negative or zero size", who);
-  if (cache_len + n_new > capacity)
-    return fail(WS_ERR_CAPACITY, "%s: cache_len %lld + n_new %lld exceeds capacity %lld", who,
+  if (n_new > capacity || cache_len > capacity - n_new)   // cache_len + n_new > capacity, without overflow
+    return fail(WS_ERR_CAPACITY,"%s: cache_len %lld + n_new %lld exceeds capacity %lld", who,
                 (long long)cache_len, (long long)n_new, (long long)capacity);
   const int64_t row_bytes = (int64_t)head_dim * (int64_t)dtype_size(dt);
   if (row_bytes % 16 != 0)

@@ -55,6 +55,11 @@ def test_kv_append_host_validation(lib):
     # capacity overflow
     st = lib.ws_kv_append(FAKE, FAKE, FAKE, FAKE, 10, 5, 12, 2, 128, ws.WS_BF16, None)
     assert st == ws.WS_ERR_CAPACITY and b"capacity" in lib.ws_last_error()
+    # cache_len + n_new past the int64 range must not wrap into an accepted write
+    big = 2 ** 63 - 1
+    assert lib.ws_kv_append(FAKE, FAKE, FAKE, FAKE, big, 1, 16, 1, 128, ws.WS_BF16, None) == ws.WS_ERR_CAPACITY
+    assert lib.ws_kv_append(FAKE, FAKE, FAKE, FAKE, 2 ** 62, 2 ** 62, 2 ** 62 + 5, 1, 128, ws.WS_BF16,
+                            None) == ws.WS_ERR_CAPACITY
     # unknown dtype
     assert lib.ws_kv_append(FAKE, FAKE, FAKE, FAKE, 0, 1, 8, 1, 64, 7, None) == ws.WS_ERR_INVALID_ARGUMENT
     # misaligned pointer
