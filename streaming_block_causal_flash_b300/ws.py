@@ -141,17 +141,32 @@ def ws_kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor
                                _dtype_code(k_new), _stream_ptr(stream)))
 
 
-def _attn(fn_name, q, k_cache, v_cache, out, offsets_host, offsets_dev, lse, softmax_scale,
-          workspace, stream):
+def _attn_shapes(q, k_cache, v_cache, out, offsets_host, offsets_dev, lse, prefill: bool):
+    """Shape checks the C ABI cannot make (it sees only pointers): the caches
+    are [H, capacity, D] and equal in shape, and q/out hold exactly the rows
+    the offsets give -- the newest block (offsets[-1] - offsets[-2] rows), or
+    every token for prefill (offsets[-1] rows).  Returns (H, cap, D, offs)."""
+    if k_cache.dim() != 3 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must both be [H, capacity, D]")
     H, cap, D = k_cache.shape
-    dt = q.dtype
     offs = _host_offsets(offsets_host)
     if offsets_dev.dtype != torch.int32 or offsets_dev.numel() != offs.size:
         raise ValueError("device offsets must be int32 with the same length as host offsets")
     if q.dim() != 3 or q.shape[1] != H or q.shape[2] != D or tuple(out.shape) != tuple(q.shape):
         raise ValueError("q/out must be [rows, H, D]")
+    rows = int(offs[-1]) if prefill else int(offs[-1]) - int(offs[-2])
+    if q.shape[0] != rows:
+        raise ValueError(f"q has {q.shape[0]} rows; the offsets give {rows}")
     if lse is not None and (lse.dtype != torch.float32 or lse.numel() != H * q.shape[0]):
         raise ValueError("lse must be float32 [H, rows]")
+    return H, cap, D, offs
+
+
+def _attn(fn_name, q, k_cache, v_cache, out, offsets_host, offsets_dev, lse, softmax_scale,
+          workspace, stream):
+    H, cap, D, offs = _attn_shapes(q, k_cache, v_cache, out, offsets_host, offsets_dev, lse,
+                                   fn_name == "ws_block_causal_prefill")
+    dt = q.dtype
     ws_ptr, ws_bytes = 0, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
@@ -181,17 +196,10 @@ def ws_block_causal_attn_side(q, k_cache, v_cache, k_side, v_side, out,
     the unit's own K/V from token-major side buffers [q_len, H, D]; with
     commit=True the kernel also writes those K/V into the cache rows of the
     last block (the append fused into the attention)."""
-    H, cap, D = k_cache.shape
+    H, cap, D, offs = _attn_shapes(q, k_cache, v_cache, out, offsets_host, offsets_dev, lse, False)
     dt = q.dtype
-    offs = _host_offsets(offsets_host)
-    if offsets_dev.dtype != torch.int32 or offsets_dev.numel() != offs.size:
-        raise ValueError("device offsets must be int32 with the same length as host offsets")
-    if q.dim() != 3 or q.shape[1] != H or q.shape[2] != D or tuple(out.shape) != tuple(q.shape):
-        raise ValueError("q/out must be [rows, H, D]")
     if tuple(k_side.shape) != tuple(q.shape) or tuple(v_side.shape) != tuple(q.shape):
         raise ValueError("k_side/v_side must be [rows, H, D] like q")
-    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != H * q.shape[0]):
-        raise ValueError("lse must be float32 [H, rows]")
     ws_ptr, ws_bytes = 0, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
@@ -209,15 +217,8 @@ def ws_block_causal_attn_noalloc(q, k_cache, v_cache, out, offsets_host: Sequenc
     """ws_block_causal_attn without a caller workspace, for callers that may
     not allocate device memory: the library's static device scratch stands in
     for it.  Calls that can overlap on the GPU race on that scratch."""
-    H, cap, D = k_cache.shape
+    H, cap, D, offs = _attn_shapes(q, k_cache, v_cache, out, offsets_host, offsets_dev, lse, False)
     dt = q.dtype
-    offs = _host_offsets(offsets_host)
-    if offsets_dev.dtype != torch.int32 or offsets_dev.numel() != offs.size:
-        raise ValueError("device offsets must be int32 with the same length as host offsets")
-    if q.dim() != 3 or q.shape[1] != H or q.shape[2] != D or tuple(out.shape) != tuple(q.shape):
-        raise ValueError("q/out must be [rows, H, D]")
-    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != H * q.shape[0]):
-        raise ValueError("lse must be float32 [H, rows]")
     _check(load().ws_block_causal_attn_noalloc(
         _dev(q, "q"), _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
         _dev(out, "out", dt), _dev(lse, "lse", torch.float32), offs.ctypes.data_as(_i32p),

@@ -211,3 +211,32 @@ int main(void) {
                           str(src), "-L", lib_dir, "-l:" + os.path.basename(ws_build.LIB_PATH),
                           "-o", str(tmp_path / "use_ws")], capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
+
+
+def test_binding_rejects_shapes_the_abi_cannot_see():
+    """The C ABI takes pointers only; the binding checks what they must hold
+    (a wrong row count or a smaller V cache would be read past its end)."""
+    import torch
+    H, D = 2, 128
+    bf = torch.bfloat16
+    k = torch.zeros(H, 64, D, dtype=bf)
+    offs = [0, 40, 60]
+    offs_dev = torch.tensor(offs, dtype=torch.int32)
+    q = torch.zeros(20, H, D, dtype=bf)
+    out = torch.empty_like(q)
+    with pytest.raises(ValueError, match="v_cache"):
+        ws.ws_block_causal_attn(q, k, torch.zeros(H, 32, D, dtype=bf), out, offs, offs_dev)
+    with pytest.raises(ValueError, match="rows"):
+        ws.ws_block_causal_attn(q[:10], k, k, out[:10], offs, offs_dev)
+    with pytest.raises(ValueError, match="rows"):
+        ws.ws_block_causal_attn_noalloc(q[:19], k, k, out[:19], offs, offs_dev)
+    with pytest.raises(ValueError, match="rows"):
+        ws.ws_block_causal_attn_side(q[:5], k, k, q[:5], q[:5], out[:5], offs, offs_dev)
+    with pytest.raises(ValueError, match="rows"):          # prefill reads all 60 tokens
+        ws.ws_block_causal_prefill(q, k, k, out, offs, offs_dev)
+    # consistent shapes get past the shape checks (and stop at the device check here)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ws.ws_block_causal_attn(q, k, k, out, offs, offs_dev)
+    full = torch.zeros(60, H, D, dtype=bf)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ws.ws_block_causal_prefill(full, k, k, torch.empty_like(full), offs, offs_dev)
