@@ -551,6 +551,24 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def host_cpu() -> dict:
+    """The host the oracle runs on: CPU model and the cores this process may use."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        affinity = os.cpu_count() or 1
+    return {"cpu_model": model, "affinity_cores": affinity}
+
+
 def oracle_unit_sample(sess: UnitSession, u: int, n_rows: int, heads=None):
     """Time the oracle on a row sample of unit u; returns (seconds, flops)."""
     from oracle import block_causal as bc
@@ -595,7 +613,7 @@ def cpu_baseline(sess: UnitSession):
     n_rows = 64
     dt, flops, rows, heads = oracle_unit_sample(sess, u, n_rows)
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": blas_threads(),
-            "kind": "oracle",
+            "kind": "oracle", **host_cpu(),
             "sample": f"fp64 numpy oracle, block-causal attention of {rows} evenly spaced query rows x "
                       f"{heads} heads of unit {u} against {int(sess.offsets_all[u + 1])} keys "
                       f"({flops / 1e9:.1f} GFLOP in {dt:.2f} s)"}
@@ -630,6 +648,7 @@ def reference_arm(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w, sess, u),
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             **host_cpu(),
                              "sample": f"per step: fp64 oracle attention of {n_rows} query rows x {len(heads)} heads "
                                        f"(extrapolated to the unit's {n} rows x {w.heads} heads) + "
                                        f"{w.euler_steps} full Euler steps"},
