@@ -1,0 +1,70 @@
+"""Build-quality checks on the CUDA sources (CPU only: nvcc cross-compiles
+for sm_103a).  The hot-path kernels compile without register spills, and the
+tensor-core attention's warpgroup register split fits in the registers its
+block is launched with (setmaxnreg.inc would otherwise wait forever; the host
+also refuses such a launch)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+from streaming_block_causal_flash_b300 import build as ws_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "streaming_block_causal_flash_b300", "csrc")
+
+
+def ptxas_report(src: str, tmp_path):
+    """{kernel name: (registers, spill store bytes, spill load bytes)}."""
+    cmd = [ws_build.nvcc_path(), "-O3", "-std=c++17", *ws_build.ARCH_FLAGS, "-Xptxas", "-v",
+           "-I", os.path.join(ROOT, "include"), "-c", src, "-o", str(tmp_path / "k.o")]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-3000:]
+    out, name = {}, None
+    spills = (0, 0)
+    for line in (res.stdout + res.stderr).splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            name = m.group(1)
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and name:
+            spills = (int(m.group(1)), int(m.group(2)))
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and name:
+            out[name] = (int(m.group(1)), *spills)
+            name, spills = None, (0, 0)
+    return out
+
+
+# Spill bytes allowed per source.  The hot path (tensor-core attention and
+# combine, append, Euler) must not spill at all.  The fp32 CUDA-core attention,
+# which serves only the tiny fp32 workload, stores and reloads 8 bytes in its
+# head_dim-128 variant; the bound keeps that from growing unnoticed.
+SPILL_ALLOWED = {"attn_simt.cu": 8}
+
+
+@pytest.mark.parametrize("src", sorted(f for f in os.listdir(CSRC) if f.endswith(".cu")))
+def test_kernels_compile_without_spills(src, tmp_path):
+    report = ptxas_report(os.path.join(CSRC, src), tmp_path)
+    allowed = SPILL_ALLOWED.get(src, 0)
+    for name, (regs, st, ld) in report.items():
+        assert st <= allowed and ld <= allowed, f"{src}: {name} spills ({st} B stored, {ld} B loaded)"
+
+
+def test_attention_register_split_fits_the_launch(tmp_path):
+    src = os.path.join(CSRC, "attn_tcgen05.cu")
+    text = open(src).read()
+    consts = {k: int(v) for k, v in re.findall(r"constexpr int (REGS_SOFTMAX|REGS_OTHER|NUM_THREADS) = (\d+);",
+                                                text)}
+    assert set(consts) == {"REGS_SOFTMAX", "REGS_OTHER", "NUM_THREADS"}
+    report = ptxas_report(src, tmp_path)
+    regs = [r for name, (r, _, _) in report.items() if "attn_tc_bf16_kernel" in name]
+    assert len(regs) == 1
+    # two softmax warpgroups grow, the third shrinks; setmaxnreg takes multiples of 8
+    need = 256 * consts["REGS_SOFTMAX"] + 128 * consts["REGS_OTHER"]
+    assert consts["NUM_THREADS"] == 384
+    assert consts["REGS_SOFTMAX"] % 8 == 0 and consts["REGS_OTHER"] % 8 == 0
+    assert need <= regs[0] * consts["NUM_THREADS"], f"split needs {need}, launch has {regs[0] * 384}"
