@@ -271,7 +271,10 @@ WS_API const char* ws_last_error(void);
  * Device error word written by the attention kernels when a bounded wait
  * gives up (they then stop, release their tensor memory and return).
  * Synchronises the current device.  *code_out = 0 when clean; otherwise the
- * call returns WS_ERR_TIMEOUT and *info_out says where (role << 8 | block).
+ * call returns WS_ERR_TIMEOUT and *info_out says where: (wait site << 16) |
+ * (block index & 0xFFFF), the first wait to give up.  The outputs of a launch
+ * that gave up are undefined; the context stays usable.  The word stays set
+ * until ws_clear_device_error().
  */
 WS_API ws_status ws_get_device_error(int* code_out, int* info_out);
 WS_API ws_status ws_clear_device_error(void);
