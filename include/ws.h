@@ -272,9 +272,14 @@ WS_API const char* ws_last_error(void);
  * gives up (they then stop, release their tensor memory and return).
  * Synchronises the current device.  *code_out = 0 when clean; otherwise the
  * call returns WS_ERR_TIMEOUT and *info_out says where: (wait site << 16) |
- * (block index & 0xFFFF), the first wait to give up.  The outputs of a launch
- * that gave up are undefined; the context stays usable.  The word stays set
- * until ws_clear_device_error().
+ * (block index & 0xFFFF), the first wait to give up.  Wait sites: 1 producer
+ * waiting for the Q slot, 2 producer waiting for a K/V slot, 3 MMA issuer
+ * waiting for Q, 4 MMA issuer (or the commit's store warp) waiting for a K/V
+ * tile, 5 MMA issuer waiting for P, 6 for the O accumulator to be free,
+ * 7 softmax waiting for S, 8 for the final O, 9 teardown waiting for
+ * MMAs, 10 for copies, 11 the test hook's stalled wait, 12 the MMA issue
+ * lock.  The outputs of a launch that gave up are undefined; the context
+ * stays usable.  The word stays set until ws_clear_device_error().
  */
 WS_API ws_status ws_get_device_error(int* code_out, int* info_out);
 WS_API ws_status ws_clear_device_error(void);
