@@ -101,18 +101,142 @@ def load_peaks():
             "source": "fallback"}
 
 
+class _CtypesNvml:
+    """The few read-only NVML queries the clock sampler makes, called through
+    ctypes on the driver's libnvidia-ml.so.1 (for hosts without the pynvml
+    package).  Names and reason bits follow NVML's public header."""
+
+    NVML_CLOCK_SM = 1
+    nvmlClocksEventReasonSwPowerCap = 0x4
+    nvmlClocksEventReasonHwSlowdown = 0x8
+    nvmlClocksEventReasonSwThermalSlowdown = 0x20
+    nvmlClocksEventReasonHwThermalSlowdown = 0x40
+
+    def __init__(self):
+        import ctypes
+        self._c = ctypes
+        self._lib = ctypes.CDLL("libnvidia-ml.so.1")
+
+    def _call(self, name, *args):
+        rc = getattr(self._lib, name)(*args)
+        if rc != 0:
+            raise RuntimeError(f"{name} returned NVML error {rc}")
+
+    def nvmlInit(self):
+        self._call("nvmlInit_v2")
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self._c.c_void_p()
+        self._call("nvmlDeviceGetHandleByPciBusId_v2", self._c.c_char_p(bus.encode()), self._c.byref(h))
+        return h
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        h = self._c.c_void_p()
+        self._call("nvmlDeviceGetHandleByIndex_v2", self._c.c_uint(i), self._c.byref(h))
+        return h
+
+    def _uint(self, name, h, *extra):
+        v = self._c.c_uint()
+        self._call(name, h, *extra, self._c.byref(v))
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, kind):
+        return self._uint("nvmlDeviceGetClockInfo", h, self._c.c_int(kind))
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind):
+        return self._uint("nvmlDeviceGetMaxClockInfo", h, self._c.c_int(kind))
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        return self._uint("nvmlDeviceGetPowerUsage", h)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self._c.c_ulonglong()
+        fn = "nvmlDeviceGetCurrentClocksEventReasons"
+        if not hasattr(self._lib, fn):
+            fn = "nvmlDeviceGetCurrentClocksThrottleReasons"
+        self._call(fn, h, self._c.byref(v))
+        return v.value
+
+    nvmlDeviceGetCurrentClocksThrottleReasons = nvmlDeviceGetCurrentClocksEventReasons
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled while the GPU is busy."""
+    """SM clock and clock-event (throttle) reasons of the GPU while it works.
+
+    A thread polls NVML every 2 ms from start() to stop(); start() also takes
+    one snapshot at once and stop() one more, so even a timed region of a few
+    milliseconds carries samples.  The host thread that launched the work is
+    then blocked in a device synchronisation (the GIL is free), which is when
+    the samples are taken.  Falls back to an `nvidia-smi -lms` stream when
+    NVML cannot be used."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
         self.gpu = gpu_index
+        self.period = period_s
         self.proc = None
+        self.thread = None
+        self.samples = []
+        self.nvml = None
+        self.handle = None
+
+    def _nvml_handle(self):
+        try:
+            import pynvml
+        except ImportError:
+            pynvml = _CtypesNvml()
+        pynvml.nvmlInit()
+        try:
+            p = torch.cuda.get_device_properties(self.gpu)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+            return pynvml, pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            return pynvml, pynvml.nvmlDeviceGetHandleByIndex(self.gpu)
+
+    def _sample(self):
+        nv, h = self.nvml, self.handle
+        sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+        mx = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        try:
+            mask = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+        except Exception:
+            mask = nv.nvmlDeviceGetCurrentClocksThrottleReasons(h)
+        try:
+            watts = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+        except Exception:
+            watts = None
+        reasons = [name for name, attr in self.REASONS if mask & getattr(nv, attr, 0)]
+        self.samples.append((float(sm), float(mx), reasons, watts))
 
     def start(self):
+        import threading
+        self.samples = []
+        self.nvml_error = None
+        try:
+            self.nvml, self.handle = self._nvml_handle()
+            self._sample()
+        except Exception as e:     # noqa: BLE001 -- any NVML failure: use nvidia-smi
+            self.nvml = None
+            self.nvml_error = f"{type(e).__name__}: {e}"[:200]
+        if self.nvml is not None:
+            self.stop_flag = threading.Event()
+
+            def loop():
+                while not self.stop_flag.wait(self.period):
+                    try:
+                        self._sample()
+                    except Exception:
+                        break
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
@@ -122,6 +246,22 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            try:
+                self._sample()
+            except Exception:
+                pass
+            sms = [x[0] for x in self.samples]
+            reasons = sorted({r for x in self.samples for r in x[2]})
+            watts = [x[3] for x in self.samples if x[3] is not None]
+            return {"sm_mhz": statistics.median(sms) if sms else None,
+                    "sm_max_mhz": max(x[1] for x in self.samples) if self.samples else None,
+                    "sm_mhz_min": min(sms) if sms else None,
+                    "power_w_median": round(statistics.median(watts), 1) if watts else None,
+                    "reasons": reasons, "samples": len(sms),
+                    "source": f"NVML every {self.period * 1e3:.0f} ms plus snapshots at start and stop"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
@@ -146,7 +286,15 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sms) if sms else None,
                 "sm_max_mhz": max(maxes) if maxes else None,
-                "reasons": sorted(reasons), "samples": len(sms)}
+                "reasons": sorted(reasons), "samples": len(sms), "source": "nvidia-smi -lms 100",
+                "nvml_error": self.nvml_error}
+
+
+def clock_normalised(ms: float, clk: dict):
+    """ms x median SM MHz (thousands of SM cycles), to compare runs at different clocks."""
+    if not clk or not clk.get("sm_mhz"):
+        return None
+    return round(ms * clk["sm_mhz"], 1)
 
 
 def source_digest(path: str) -> str:
@@ -269,7 +417,7 @@ def run_unit(sess: UnitSession, u: int, stream, ev=None):
 
 # ------------------------------------------------------------- native arm
 
-def time_native(args, sess: UnitSession, device, world):
+def time_native(args, sess: UnitSession, device, world, clocks=None):
     stream = torch.cuda.current_stream(device)
     units = sess.units
     K, W = args.steps, args.warmup
@@ -280,6 +428,8 @@ def time_native(args, sess: UnitSession, device, world):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world, device)
     torch.cuda.synchronize(device)
+    if clocks is not None:
+        clocks.start()
     start.record(stream)
     flops = 0.0
     for i in range(K):
@@ -288,12 +438,14 @@ def time_native(args, sess: UnitSession, device, world):
         flops += sess.unit_flops(u)
     stop.record(stream)
     torch.cuda.synchronize(device)
+    clk = clocks.stop() if clocks is not None else None
     barrier(world, device)
     total_ms = start.elapsed_time(stop)
     append_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     euler_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    return total_ms, flops, append_ms, attn_ms, euler_ms
+    unit_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    return total_ms, flops, append_ms, attn_ms, euler_ms, unit_ms, clk
 
 
 def time_e2e(args, sess: UnitSession, device):
@@ -438,7 +590,22 @@ def time_hbm_kernels(sess: UnitSession, device, peaks):
     byts = 4.0 * slice_bytes
     out = {"append": {"us": round(us, 2), "bytes": int(byts), "gbs": round(byts / us / 1e3, 1),
                       "frac_hbm": round(byts / us / 1e3 / peaks["hbm_gbs"], 3)}}
-    del ks, vs
+    # The ceiling for one standalone launch that moves this many bytes: a
+    # plain device-to-device copy (cudaMemcpyAsync) of the same 2 x slice
+    # bytes (read once, written once), timed the same way.
+    src = [torch.empty(2 * slice_bytes, dtype=torch.uint8, device=device) for _ in range(nsets)]
+    dst = [torch.empty(2 * slice_bytes, dtype=torch.uint8, device=device) for _ in range(nsets)]
+
+    def copy(i, st):
+        with torch.cuda.stream(st):
+            dst[(i + 1) % nsets].copy_(src[i % nsets], non_blocking=True)
+
+    us_c = graph_time_us(copy, 8 * nsets, device)
+    out["same_size_copy"] = {"us": round(us_c, 2), "bytes": int(byts), "gbs": round(byts / us_c / 1e3, 1),
+                             "frac_hbm": round(byts / us_c / 1e3 / peaks["hbm_gbs"], 3),
+                             "what": "one device-to-device cudaMemcpyAsync of the K+V slice bytes"}
+    out["append"]["frac_of_same_size_copy"] = round(us_c / us, 3)
+    del ks, vs, src, dst
     nl = w.latent_tokens * w.latent_channels
     per = nl * (4 + 2 + 4)
     zsets = max(4, int(3 * L2_BYTES // per) + 1)
@@ -462,7 +629,7 @@ def time_hbm_kernels(sess: UnitSession, device, peaks):
                         "frac_hbm": round(per_cfg / us / 1e3 / peaks["hbm_gbs"], 3)}
     out["method"] = (f"back-to-back launches replayed from a CUDA graph, mean per launch; rotating "
                      f"{nsets} (append) / {zsets} (Euler) buffer sets, 3x L2 in total; "
-                     f"peak = measured HBM copy bandwidth")
+                     f"peak = {peaks['source']} HBM copy bandwidth")
     return out
 
 
@@ -496,9 +663,10 @@ def time_attn_side(sess: UnitSession, device, peaks, reps: int = 20):
 def time_fused_unit(sess: UnitSession, device, reps: int = 50, rounds: int = 3):
     """The unit step with the append fused into the attention (one
     ws_block_causal_attn_side call that reads the unit's K/V from its slice
-    and commits them to the cache, then the Euler steps) against the plain
-    step (append, attention, Euler steps).  Both graph-replayed, measured in
-    alternation so that they see the same clocks; the best round of each."""
+    and, in the background, commits them to the cache; then the Euler steps)
+    against the plain step (append, attention, Euler steps).  Both
+    graph-replayed, measured in alternation so that they see the same clocks;
+    the best round of each."""
     from streaming_block_causal_flash_b300 import ws
     u = sess.units[0]
     n = sess.sizes[u]
@@ -608,9 +776,12 @@ def oracle_step_rest(sess: UnitSession, u: int):
     return time.perf_counter() - t0
 
 
+REFERENCE_ROWS = 64
+
+
 def cpu_baseline(sess: UnitSession):
     u = sess.units[0]
-    n_rows = 64
+    n_rows = REFERENCE_ROWS
     dt, flops, rows, heads = oracle_unit_sample(sess, u, n_rows)
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": blas_threads(),
             "kind": "oracle", **host_cpu(),
@@ -627,31 +798,37 @@ def reference_arm(args, rank, world):
         raise SystemExit("--impl reference times the oracle on the streaming-unit workloads only")
     sess = UnitSession(w, None, host_only=True)
     u = sess.units[0]
-    offs = sess.offsets_all[:u + 2]
     n = sess.sizes[u]
-    heads = list(range(min(8, w.heads)))
-    n_rows = 8
-    times = []
+    # Each step is one measured run of the oracle on a named, bounded sample
+    # of the unit: its attention for n_rows evenly spaced query rows x every
+    # head.  value and ms_per_step are that measurement, nothing scaled.  A
+    # long run (more than 60 steps) takes a quarter of the rows per step so
+    # that it still ends within a few minutes.
+    n_rows = REFERENCE_ROWS if args.steps + args.warmup <= 60 else REFERENCE_ROWS // 4
+    times, flops_s, rows = [], 0.0, 0
     for i in range(args.warmup + args.steps):
-        dt_attn, flops_s, rows, nh = oracle_unit_sample(sess, u, n_rows, heads)
-        dt_rest = oracle_step_rest(sess, u)
-        # extrapolate the attention sample to the whole unit (rows x heads)
-        unit_ms = (dt_attn * (n / rows) * (w.heads / nh) + dt_rest) * 1e3
+        dt_attn, flops_s, rows, nh = oracle_unit_sample(sess, u, n_rows)
         if i >= args.warmup:
-            times.append(unit_ms)
+            times.append(dt_attn * 1e3)
     ms = statistics.mean(times)
-    value = sess.unit_flops(u) / (ms * 1e-3) / 1e12
+    value = flops_s / (ms * 1e-3) / 1e12
+    euler_ms = oracle_step_rest(sess, u) * 1e3
     cores = blas_threads()
+    sample = (f"per step: fp64 numpy oracle, block-causal attention of {rows} evenly spaced query rows x "
+              f"{w.heads} heads of unit {u} against {int(sess.offsets_all[u + 1])} keys "
+              f"({flops_s / 1e9:.1f} GFLOP)")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w, sess, u),
+            "step_sample": sample,
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             **host_cpu(),
-                             "sample": f"per step: fp64 oracle attention of {n_rows} query rows x {len(heads)} heads "
-                                       f"(extrapolated to the unit's {n} rows x {w.heads} heads) + "
-                                       f"{w.euler_steps} full Euler steps"},
+                             **host_cpu(), "sample": sample},
+            "extrapolated": {"unit_ms": round(ms * (n / rows) + euler_ms, 1),
+                             "what": f"the sample's time scaled to the unit's {n} query rows, plus "
+                                     f"{w.euler_steps} oracle Euler steps over the full latents "
+                                     f"({euler_ms:.1f} ms, measured once): an estimate, not a measurement"},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -794,9 +971,8 @@ def main(argv=None):
         return prefill_main(args, w, device, rank, world, peaks)
     sess = UnitSession(w, device)
     clocks = ClockSampler(local)
-    clocks.start()
-    total_ms, flops, append_ms, attn_ms, euler_ms = time_native(args, sess, device, world)
-    clk = clocks.stop()
+    total_ms, flops, append_ms, attn_ms, euler_ms, unit_ms, clk = time_native(
+        args, sess, device, world, clocks)
     code, info = ws.ws_get_device_error()
     if code != 0:
         raise SystemExit(f"device error word set during the timed region: {info:#x}")
@@ -815,8 +991,18 @@ def main(argv=None):
                 "traffic": recorded_traffic(w.name),
                 "kernel": "attn_tc_bf16_kernel (+ attn_combine_kernel) = one ws_block_causal_attn call",
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
-                if peaks["source"] == "measured" else "fallback 1.8 PFLOP/s",
+                if peaks["source"] == "measured" else "fallback 1.8 PFLOP/s (no MEASURED_PEAKS.json)",
                 "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+    per_unit = {"mean": round(statistics.mean(unit_ms), 4), "p50": round(statistics.median(unit_ms), 4),
+                "max": round(max(unit_ms), 4), "min": round(min(unit_ms), 4),
+                "units": len(sess.units),
+                "what": "device time of each timed step (append + attention + Euler steps of one "
+                        "unit, CUDA events on the launching stream); the steps cycle over the "
+                        f"workload's {len(sess.units)} new unit(s)"}
+    if len(sess.units) > 1:
+        per_unit["by_unit_mean"] = {str(u): round(statistics.mean(
+            unit_ms[i] for i in range(K) if sess.units[i % len(sess.units)] == u), 4)
+            for u in sess.units if any(sess.units[i % len(sess.units)] == u for i in range(K))}
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(max_ms, 4),
             "us_per_unit": round(max_ms * 1e3, 1), "higher_is_better": True, "scaling": "weak",
@@ -826,7 +1012,9 @@ def main(argv=None):
             "gpu_launches": sess.launches_per_step() * K, "clocks": clk,
             "kernels_ms_mean": {"kv_append": round(statistics.mean(append_ms), 4),
                                 "block_causal_attn": round(attn_avg_ms, 4),
-                                "fm_euler_steps": round(statistics.mean(euler_ms), 4)}}
+                                "fm_euler_steps": round(statistics.mean(euler_ms), 4)},
+            "per_unit_ms": per_unit,
+            "attn_ms_x_sm_mhz": clock_normalised(attn_avg_ms, clk)}
     if not args.no_e2e:
         e2e = time_e2e(args, sess, device)
         e_ms, e_flops = reduce_over_ranks(e2e["ms_per_step"], sess.unit_flops(sess.units[0]), world, device)

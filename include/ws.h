@@ -212,8 +212,11 @@ WS_API ws_status ws_fm_euler_step(void* z, ws_dtype z_dt, const void* v, ws_dtyp
  *    saying so; nothing is launched.  40 MiB covers every unit call on a GPU
  *    of up to 158 SMs (a B300 has 148).
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make that
- *    first call before any stream capture on the device.
+ *    (cudaGetSymbolAddress, with that device current) and caches it together
+ *    with the id of the current context; make that first call before any
+ *    stream capture on the device.  If the context is replaced (for example
+ *    after cudaDeviceReset), the next call looks the address up again in the
+ *    new context, so that call too belongs before any stream capture.
  *  - All calls on a device share the one array.  Its contents on entry do not
  *    matter (every value read is written earlier in the same call), but two
  *    calls that may overlap on the GPU -- on different streams, or from
@@ -274,11 +277,12 @@ WS_API const char* ws_last_error(void);
  * call returns WS_ERR_TIMEOUT and *info_out says where: (wait site << 16) |
  * (block index & 0xFFFF), the first wait to give up.  Wait sites: 1 producer
  * waiting for the Q slot, 2 producer waiting for a K/V slot, 3 MMA issuer
- * waiting for Q, 4 MMA issuer (or the commit's store warp) waiting for a K/V
- * tile, 5 MMA issuer waiting for P, 6 for the O accumulator to be free,
- * 7 softmax waiting for S, 8 for the final O, 9 teardown waiting for
- * MMAs, 10 for copies, 11 the test hook's stalled wait, 12 the MMA issue
- * lock.  The outputs of a launch that gave up are undefined; the context
+ * waiting for Q, 4 MMA issuer waiting for a K/V tile, 5 MMA issuer waiting
+ * for P, 6 for the O accumulator to be free, 7 softmax waiting for S, 8 for
+ * the final O, 9 teardown waiting for MMAs, 10 for copies, 11 the test
+ * hook's stalled wait, 12 the MMA issue lock, 13 the commit copy of
+ * ws_block_causal_attn_side waiting for the producer's progress.  The
+ * outputs of a launch that gave up are undefined; the context
  * stays usable.  The word stays set until ws_clear_device_error().
  */
 WS_API ws_status ws_get_device_error(int* code_out, int* info_out);
@@ -286,7 +290,10 @@ WS_API ws_status ws_clear_device_error(void);
 
 /*
  * Limit, in nanoseconds, of every in-kernel wait launched after this call
- * (default 2e9).  Host-side setting, process wide.
+ * (default 2e9).  Host-side setting, process wide: it applies to calls from
+ * every thread.  Setting it is thread-safe, but a call running concurrently
+ * on another thread may use either the old or the new value, so change it
+ * while no attention call is being made.
  */
 WS_API ws_status ws_set_wait_timeout_ns(uint64_t timeout_ns);
 
@@ -297,7 +304,9 @@ WS_API ws_status ws_set_wait_timeout_ns(uint64_t timeout_ns);
  * runs out, the kernel records the wait site in the device error word, every
  * role stops, drains its own copies and MMAs, frees its tensor memory and
  * returns; ws_get_device_error() then reports WS_ERR_TIMEOUT.  Outputs of
- * such a launch are undefined.  Nothing faults, traps or hangs.
+ * such a launch are undefined.  Nothing faults, traps or hangs.  Like the
+ * wait limit it is process wide (it affects calls from every thread); switch
+ * it only while no attention call is being made.
  */
 WS_API ws_status ws_debug_force_wait_timeout(int on);
 

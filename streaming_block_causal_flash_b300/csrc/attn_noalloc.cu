@@ -13,7 +13,12 @@
 // Host code cannot use the array's name as a device address (on the host the
 // name refers to a host-side stand-in), so the device address is looked up
 // with cudaGetSymbolAddress once per device, with that device current, the
-// first time the entry point runs on it.
+// first time the entry point runs on it.  The address belongs to the device's
+// current context: if that context is destroyed and replaced (for example by
+// cudaDeviceReset), the module is loaded again at a new address.  So the
+// cached address is kept together with the unique id of the context it was
+// looked up in, and looked up again when the current context's id differs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -36,9 +41,38 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (looked up once
-// per device and cached).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if it cannot be read;
+// the cache is then keyed on the device alone).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device and context and cached.
 ws_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -50,8 +84,11 @@ ws_status scratch_address(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices)
     return ws::record_failure(WS_ERR_CUDA, "ws_block_causal_attn_noalloc: device index too large");
+  // 0 when the thread has no current context yet: the look-up below creates
+  // it, and its id is read again afterwards.
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (g_scratch_addr[dev] == nullptr || (ctx != 0 && g_scratch_ctx[dev] != ctx)) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -61,7 +98,9 @@ ws_status scratch_address(void** out) {
                cudaGetErrorString(e));
       return ws::record_failure(WS_ERR_CUDA, msg);
     }
+    if (ctx == 0) ctx = current_context_id();
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return WS_OK;

@@ -17,9 +17,10 @@
 //   warp  9    TMEM owner; its lane 0 issues every MMA of query tile 0
 //   warp  10   lane 0 issues every MMA of query tile 1 (two issuers keep the
 //              tensor pipe fed while the other one waits on barriers)
-//   warp  11   side mode with commit: copies the newest unit's K/V tiles
-//              into the cache (otherwise idle; it completes the third
-//              warpgroup, which gives up registers to the softmax warpgroups)
+//   warp  11   side mode with commit: copies this CTA's share of the newest
+//              unit's K/V slices into the cache, global to global, in the
+//              background (otherwise idle; it completes the third warpgroup,
+//              which gives up registers to the softmax warpgroups)
 // TMEM (512 columns): tile t uses S_t = cols [256t, 256t+128) (fp32 logits,
 // overwritten in place by bf16 P in its first 64 columns) and
 // O_t = cols [256t+128, 256t+256) (fp32 output accumulator).
@@ -53,7 +54,8 @@
 //    Side mode (unit mode only): keys [0, cache_len) come from the cache and
 //    the newest unit's keys from token-major side buffers through 2-D TMA
 //    maps; the two parts are tiled separately, each with its own ragged tail.
-//    With commit, warp 11 also copies the side tiles into the cache.
+//    With commit, warp 11 of every CTA also copies an equal share of the
+//    side slices into the cache, outside the K/V ring.
 //  * prefill mode: one work item per (head, query-tile pair), head-major,
 //    longest key range first; key tiles no row of a query tile can see are
 //    skipped; CTAs take items round-robin.
@@ -62,6 +64,8 @@
 // error word, stops all roles, waits (bounded) for its own copies and MMAs in
 // flight, frees its tensor memory and returns.
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "ws_internal.h"
 #include "ws_ptx.cuh"
@@ -113,12 +117,12 @@ constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = 2 * TILE_BYTES;
 constexpr int SMEM_BARS = SMEM_KV + NSTAGE * TILE_BYTES;
 constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_MISC + 16;   // tmem slot, abort flag, issue lock
+constexpr int SMEM_USED = SMEM_MISC + 16;   // tmem slot, abort flag, issue lock, loads issued
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 // wait sites (error info)
 enum : int { W_PROD_QE = 1, W_PROD_KVE, W_MMA_Q, W_MMA_KV, W_MMA_P, W_MMA_OF, W_SM_S, W_SM_O,
-             W_DRAIN_MMA, W_DRAIN_TMA, W_FORCED, W_LOCK };
+             W_DRAIN_MMA, W_DRAIN_TMA, W_FORCED, W_LOCK, W_COMMIT };
 
 struct Params {
   int prefill;
@@ -134,6 +138,8 @@ struct Params {
   int commit;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;
+  const void* k_side;   // [n_side][heads][HD], the commit's source
+  const void* v_side;
   long long capacity;
   long long work;
   int n_items;
@@ -344,6 +350,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + SMEM_MISC + 4);
   int* issue_lk = reinterpret_cast<int*>(sgen + SMEM_MISC + 8);
+  // K/V tile loads the producer has issued so far (paces the commit copy)
+  volatile int* loads_issued = reinterpret_cast<volatile int*>(sgen + SMEM_MISC + 12);
   auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x >> 5;
@@ -352,8 +360,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), 1);
-      // released by both MMA issuers (and, with commit, the store warp)
-      mbar_init(bar(BAR_KV_EMPTY + s), 2 + P.commit);
+      // released by both MMA issuers
+      mbar_init(bar(BAR_KV_EMPTY + s), 2);
     }
     mbar_init(bar(BAR_Q_FULL), 1);
     mbar_init(bar(BAR_Q_EMPTY), 2);
@@ -368,6 +376,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(BAR_STALL), 1);
     *abort_flag = 0;
     *issue_lk = 0;
+    *loads_issued = 0;
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -437,6 +446,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                             kv0, item.h);
             }
             ++issued;
+            *loads_issued = issued;
             ring.advance();
           }
         }
@@ -573,53 +583,79 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncwarp();
   } else if (warp == 11 && P.commit) {
     // -------------------------------------- store warp (side mode, commit)
-    // A third consumer of the K/V ring: it waits for every slot to fill.
-    // Side tile js of a head is copied by the group's CTA with query pair
-    // js % pairs (each tile exactly once, the work spread over the group):
-    // all 32 lanes read the 128-byte-swizzled tile from shared memory in
-    // 16-byte chunks and write them to cache rows cache_len + (side row),
-    // skipping rows past the unit.  Plain loads and stores keep the TMA unit
-    // free for the ring's loads (TMA stores measured twice as costly).  The
-    // slot is released once the copy has read it.
+    // Copies the newest block's K/V from the token-major side buffers
+    // ([n_side][H][HD]) into cache rows cache_len + t of every head, in the
+    // background: it takes no part in the K/V ring, so the attention's loads
+    // and MMAs never wait for it.  The 256-byte rows (token t, head h) of
+    // both slices, K then V, are split evenly over the CTAs.  Per iteration
+    // the warp moves 16 consecutive rows: lanes 0-15 the 16-byte columns of
+    // rows r0..r0+7, lanes 16-31 those of rows r0+8..r0+15, 8 loads in flight
+    // per lane before their stores.  The (tensor, t, h) of a lane's first row
+    // takes one division; the next rows step h with a carry, which keeps the
+    // warp's instruction count small (it shares its scheduler with softmax
+    // warps).  No row it writes is read by this launch (the cache maps end at
+    // the history), and the writes are visible once the launch ends.
+    // The copy is paced by the CTA's own progress: iteration k waits until
+    // the producer has issued a matching share of this CTA's K/V loads, so
+    // the copy's HBM traffic is spread thinly over the launch instead of
+    // competing with the loads that fill the pipeline at its start.
     {
+      constexpr int CPR = HD * 2 / 16;                         // 16-byte chunks per row
+      constexpr int ROWS = 8;
+      const long long per_tensor = static_cast<long long>(P.n_side) * P.heads;
+      const long long total = 2 * per_tensor;
+      const long long r_begin = total * blockIdx.x / gridDim.x;
+      const long long r_end = total * (blockIdx.x + 1) / gridDim.x;
+      const int col = lane & (CPR - 1);
+      const uint4* k_src = static_cast<const uint4*>(P.k_side);
+      const uint4* v_src = static_cast<const uint4*>(P.v_side);
+      uint4* k_dst = reinterpret_cast<uint4*>(P.k_cache);
+      uint4* v_dst = reinterpret_cast<uint4*>(P.v_cache);
       ItemIter it;
       iter_init(P, it);
-      Item item;
-      Ring ring;
-      bool ok = true;
-      while (ok && iter_next(P, it, item)) {
-        const int n_iter = max(item.n[0], item.n[1]);
-        for (int j = 0; j < n_iter && ok; ++j) {
-          const int tile = item.t0 + j;
-          const int js = tile - P.kv_tiles_c;
-          const bool store = js >= 0 && js % P.pairs == item.pair;
-          for (int which = 0; which < 2; ++which) {
-            const uint32_t full = bar(BAR_KV_FULL + ring.stage);
-            int got = 1;
-            if (lane == 0) got = wait_bar(full, ring.phase, abort_flag, P.timeout_ns, W_MMA_KV);
-            if (__shfl_sync(0xffffffffu, got, 0) == 0) { ok = false; break; }
-            // every lane observes the completed phase, which makes the
-            // tile's TMA writes visible to it (returns at once)
-            for (int w = 0; w < 1000000 && !mbar_try_wait(full, ring.phase); ++w) {}
-            if (store) {
-              const uint8_t* src = sgen + SMEM_KV + ring.stage * TILE_BYTES;
-              __nv_bfloat16* cache = which == 0 ? P.k_cache : P.v_cache;
-              const int rows = min(BN, P.n_side - js * BN);
-              const size_t row0 = static_cast<size_t>(item.h) * P.capacity + P.cache_len + js * BN;
-              for (int i = lane; i < 2 * BN * 8; i += 32) {
-                const int hf = i / (BN * 8);          // 64-column half
-                const int r = (i >> 3) % BN;          // key row in the tile
-                const int c = i & 7;                  // 16-byte chunk in the half-row
-                if (r < rows) {
-                  const uint4 v = *reinterpret_cast<const uint4*>(
-                      src + hf * HALF_BYTES + r * 128 + ((c ^ (r & 7)) << 4));
-                  *reinterpret_cast<uint4*>(cache + (row0 + r) * HD + hf * 64 + c * 8) = v;
-                }
-              }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_KV_EMPTY + ring.stage));
-            ring.advance();
+      const long long my_loads = 2 * (it.fe - it.fb);           // unit mode: K and V per key tile
+      const long long iters = (r_end - r_begin + 2 * ROWS - 1) / (2 * ROWS);
+      const long long head = my_loads < NSTAGE ? my_loads : NSTAGE;
+      const uint64_t t_start = global_timer_ns();
+      for (long long r0 = r_begin + ROWS * (lane >> 4); r0 < r_end; r0 += 2 * ROWS) {
+        const long long k = (r0 - r_begin) / (2 * ROWS);
+        const long long target = head + (my_loads - head) * k / iters;
+        bool go = true;
+        while (*loads_issued < target) {
+          if (*abort_flag) { go = false; break; }
+          if (global_timer_ns() - t_start > P.timeout_ns) {
+            *abort_flag = 1;
+            record_error(W_COMMIT);
+            go = false;
+            break;
+          }
+          __nanosleep(256);
+        }
+        if (!go) break;
+        // loads: row r of the slices is row r of K (r < per_tensor) or row
+        // r - per_tensor of V, contiguous in the source
+        uint4 val[ROWS];
+#pragma unroll
+        for (int u = 0; u < ROWS; ++u) {
+          const long long r = r0 + u;
+          if (r < r_end)
+            val[u] = ld_nc_na(r < per_tensor ? k_src + r * CPR + col
+                                             : v_src + (r - per_tensor) * CPR + col);
+        }
+        // stores: (tensor, t, h) of row r0 by one division, then stepped
+        int is_v = r0 >= per_tensor ? 1 : 0;
+        const long long rl = r0 - (is_v ? per_tensor : 0);
+        int t = static_cast<int>(rl / P.heads);
+        int h = static_cast<int>(rl - static_cast<long long>(t) * P.heads);
+#pragma unroll
+        for (int u = 0; u < ROWS; ++u) {
+          if (r0 + u < r_end) {
+            uint4* dst = is_v ? v_dst : k_dst;
+            dst[(static_cast<long long>(h) * P.capacity + P.cache_len + t) * CPR + col] = val[u];
+          }
+          if (++h == P.heads) {
+            h = 0;
+            if (++t == P.n_side) { t = 0; is_v = 1; }
           }
         }
       }
@@ -966,21 +1002,28 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                                 const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s) {
+  // One-time set-up per device (shared-memory opt-in, register-split check),
+  // under a lock so that threads making their first call at once do it once.
+  static std::mutex setup_mu;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && !attr_done[dev]) {
-    err = cudaFuncSetAttribute(attn_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_ALLOC);
-    if (err != cudaSuccess) return err;
-    // The warpgroup register split must fit in the registers the block is
-    // launched with, or setmaxnreg.inc would wait forever: refuse instead.
-    cudaFuncAttributes fa{};
-    err = cudaFuncGetAttributes(&fa, attn_tc_bf16_kernel);
-    if (err != cudaSuccess) return err;
-    if (fa.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
-    attr_done[dev] = true;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(setup_mu);
+    if (!attr_done[dev]) {
+      err = cudaFuncSetAttribute(attn_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_ALLOC);
+      if (err != cudaSuccess) return err;
+      // The warpgroup register split must fit in the registers the block is
+      // launched with, or setmaxnreg.inc would wait forever: refuse instead.
+      cudaFuncAttributes fa{};
+      err = cudaFuncGetAttributes(&fa, attn_tc_bf16_kernel);
+      if (err != cudaSuccess) return err;
+      if (fa.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
+      attr_done[dev] = true;
+    }
   }
   Params P{};
   P.prefill = plan.prefill;
@@ -998,6 +1041,8 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   P.commit = (plan.side_len > 0 && a.commit) ? 1 : 0;
   P.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.k_cache));
   P.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.v_cache));
+  P.k_side = a.k_side;
+  P.v_side = a.v_side;
   P.capacity = a.capacity;
   P.groups = plan.groups;
   P.work = plan.work;

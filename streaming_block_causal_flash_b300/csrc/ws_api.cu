@@ -4,6 +4,7 @@
 // launches nothing and touches no memory.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -16,8 +17,11 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
-uint64_t g_timeout_ns = 2000000000ull;
-int g_force_stall = 0;
+// Process-wide settings read by every attention call on any thread.  Atomic
+// (relaxed: each value stands alone), so a setter racing a call is not a data
+// race; a call uses whichever value it reads at its start.
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_force_stall{0};
 
 ws_status fail(ws_status s, const char* fmt, ...) {
   va_list ap;
@@ -229,10 +233,12 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   a.capacity = capacity;
   a.scale = scale;
   a.workspace = workspace;
-  a.force_stall = g_force_stall;
+  a.force_stall = g_force_stall.load(std::memory_order_relaxed);
   a.commit = (side && commit) ? 1 : 0;
-  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs, g_timeout_ns,
-                                          stream);
+  a.k_side = k_side;
+  a.v_side = v_side;
+  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs,
+                                          g_timeout_ns.load(std::memory_order_relaxed), stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
 }
@@ -267,12 +273,12 @@ const char* ws_last_error(void) { return g_last_error; }
 
 ws_status ws_set_wait_timeout_ns(uint64_t timeout_ns) {
   if (timeout_ns == 0) return fail(WS_ERR_INVALID_ARGUMENT, "ws_set_wait_timeout_ns: must be > 0");
-  g_timeout_ns = timeout_ns;
+  g_timeout_ns.store(timeout_ns, std::memory_order_relaxed);
   return ok();
 }
 
 ws_status ws_debug_force_wait_timeout(int on) {
-  g_force_stall = on ? 1 : 0;
+  g_force_stall.store(on ? 1 : 0, std::memory_order_relaxed);
   return ok();
 }
 

@@ -80,6 +80,8 @@ struct TcAttnArgs {
   void* workspace;
   int force_stall;       // test hook (ws_debug_force_wait_timeout)
   int commit;            // side mode: also write the side K/V into the cache
+  const void* k_side;    // side mode: the newest block's K/V, [q_len][H][128] (commit source)
+  const void* v_side;
 };
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -264,6 +264,16 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
+// 16-byte global load through the non-coherent path, not kept in L1 (data
+// read once).
+__device__ __forceinline__ uint4 ld_nc_na(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // --------------------------------------------------------------- scalars
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

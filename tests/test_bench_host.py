@@ -84,7 +84,10 @@ def test_reference_arm_under_torchrun_two_ranks(tmp_path):
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(root, "bench.py"),
            "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
            "--workload", "unit_192x336"]
+    import time
+    t0 = time.time()
     res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    wall = time.time() - t0
     assert res.returncode == 0, res.stderr[-2000:]
     lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -92,3 +95,39 @@ def test_reference_arm_under_torchrun_two_ranks(tmp_path):
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["cpu_baseline"]["affinity_cores"] >= 1 and line["cpu_baseline"]["cpu_model"]
+    # the step time is a measurement of the named sample: it fits in the run
+    assert line["ms_per_step"] * (line["steps"] + line["warmup"]) / 1e3 < wall
+    assert line["cpu_baseline"]["value"] == line["value"] and "step_sample" in line
+
+
+def test_clock_sampler_reads_nvml_snapshots_and_reasons(monkeypatch):
+    """With NVML available the sampler records a snapshot at start and stop
+    (so a timed region of a few milliseconds still carries samples) and
+    reports the median SM clock, the maximum and the active reasons."""
+    import sys
+    import types
+    import time
+
+    clocks = iter([1900, 1950, 2000] + [2000] * 10000)
+    fake = types.SimpleNamespace(
+        NVML_CLOCK_SM=1,
+        nvmlClocksEventReasonHwSlowdown=0x8, nvmlClocksEventReasonHwThermalSlowdown=0x40,
+        nvmlClocksEventReasonSwThermalSlowdown=0x20, nvmlClocksEventReasonSwPowerCap=0x4,
+        nvmlInit=lambda: None,
+        nvmlDeviceGetHandleByPciBusId=lambda bus: "h",
+        nvmlDeviceGetHandleByIndex=lambda i: "h",
+        nvmlDeviceGetClockInfo=lambda h, kind: next(clocks),
+        nvmlDeviceGetMaxClockInfo=lambda h, kind: 2032,
+        nvmlDeviceGetCurrentClocksEventReasons=lambda h: 0x4,
+        nvmlDeviceGetPowerUsage=lambda h: 900000,
+    )
+    monkeypatch.setitem(sys.modules, "pynvml", fake)
+    s = bench.ClockSampler(0, period_s=0.001)
+    s.start()
+    time.sleep(0.01)
+    out = s.stop()
+    assert out["samples"] >= 2
+    assert out["sm_max_mhz"] == 2032 and out["reasons"] == ["sw_power_cap"]
+    assert 1900 <= out["sm_mhz"] <= 2000 and out["power_w_median"] == 900.0
+    assert bench.clock_normalised(2.0, out) == round(2.0 * out["sm_mhz"], 1)
+    assert bench.clock_normalised(2.0, {"sm_mhz": None}) is None

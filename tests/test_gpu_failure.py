@@ -51,7 +51,7 @@ def test_wait_limit_reports_timeout_and_context_survives():
         ws.ws_set_wait_timeout_ns(DEFAULT_LIMIT_NS)
     assert code == 1, "the stalled wait must give up"
     site, block = info >> 16, info & 0xFFFF
-    assert 1 <= site <= 12, f"unknown wait site {site}"
+    assert 1 <= site <= 13, f"unknown wait site {site}"
     assert block < 148 * 4
     with pytest.raises(ws.WsError) as ei:
         ws._check(ws.load().ws_get_device_error(*(ws.ctypes.byref(ws.ctypes.c_int()) for _ in range(2))))
