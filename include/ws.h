@@ -137,9 +137,10 @@ WS_API ws_status ws_block_causal_attn(const void* q, const void* k_cache, const 
  * commit          0: the cache is not written.  Nonzero: the kernel also
  *                 writes the side K/V into cache rows [offsets[n_blocks-1],
  *                 offsets[n_blocks]) of every head -- the same bytes
- *                 ws_kv_append would write, from the tiles it has already
- *                 loaded (the append fused into the attention); the solver's
- *                 last step commits the clean slice this way.  Requires
+ *                 ws_kv_append would write (the append fused into the
+ *                 attention: one warp of every CTA copies an equal share of
+ *                 the slices while the attention runs); the solver's last
+ *                 step commits the clean slice this way.  Requires
  *                 offsets[n_blocks] <= capacity.
  * The cache must hold blocks 0..n_blocks-2 (offsets[n_blocks-1] <= capacity,
  * else WS_ERR_CAPACITY); rows from offsets[n_blocks-1] on are not read.

@@ -88,8 +88,8 @@ constexpr int NUM_THREADS = 384;
 // the producer/MMA warpgroup shrinks to REGS_OTHER.  The sum must fit in what
 // the block is launched with (NUM_THREADS x the kernel's register count); the
 // host checks that before every launch.
-constexpr int REGS_SOFTMAX = 200;
-constexpr int REGS_OTHER = 96;
+constexpr int REGS_SOFTMAX = 216;
+constexpr int REGS_OTHER = 72;
 constexpr int REGS_NEEDED = 256 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -601,7 +601,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // competing with the loads that fill the pipeline at its start.
     {
       constexpr int CPR = HD * 2 / 16;                         // 16-byte chunks per row
-      constexpr int ROWS = 8;
+      constexpr int ROWS = 4;
       const long long per_tensor = static_cast<long long>(P.n_side) * P.heads;
       const long long total = 2 * per_tensor;
       const long long r_begin = total * blockIdx.x / gridDim.x;
@@ -718,52 +718,61 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         // intact in TMEM then, because P is stored only after the check.
         const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
         uint64_t lsum[2];
+        // One instance of the exponential pass serves both attempts: the
+        // fast one against the current max, and (at most once, if the fast
+        // one overflowed or the rows have no max yet) the exact one after
+        // the tile max and the rescale.  A second copy of the pass in the
+        // code measured about 1.5% slower.
         bool exact = __any_sync(0xffffffffu, m == -INFINITY);
-        if (!exact) {
-          exp_pass(s, sc2, m, lsum);
+#pragma unroll 1
+        for (;;) {
+          if (exact) {
+            const float m_tile = tile_max(s) * P.scale_log2;
+            const bool need = m_tile > m + RESCALE_LOG2;
+            if (__any_sync(0xffffffffu, need)) {
+              const float m_new = need ? m_tile : m;
+              const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+              if (jj > 0) {
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                  uint32_t o[16];
+                  tmem_ld16(tO + 16u * c, o);
+                  tmem_ld_wait16(o);
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st16(tO + 16u * c, o);
+                }
+              }
+              l *= alpha;
+              m = m_new;
+            }
+          }
+          exp_pass(s, sc2, (m == -INFINITY) ? 0.f : m, lsum);
+          if (exact) break;
           float a0, a1, b0, b1;
           f2_unpack(lsum[0], a0, a1);
           f2_unpack(lsum[1], b0, b1);
           const float tile_sum = (a0 + a1) + (b0 + b1);
-          if (__any_sync(0xffffffffu, !(tile_sum <= SPEC_SUM_LIMIT))) {
+          if (!__any_sync(0xffffffffu, !(tile_sum <= SPEC_SUM_LIMIT))) break;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s[c]);
-            tmem_ld_wait_only();
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s[c]);
+          tmem_ld_wait_only();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
-            mask_tail(s, kv0, e_lim);
-            exact = true;
-          }
+          for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
+          mask_tail(s, kv0, e_lim);
+          exact = true;
         }
-        if (exact) {
-          const float m_tile = tile_max(s) * P.scale_log2;
-          const bool need = m_tile > m + RESCALE_LOG2;
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = need ? m_tile : m;
-            const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-            if (jj > 0) {
-#pragma unroll 1
-              for (int c = 0; c < 8; ++c) {
-                uint32_t o[16];
-                tmem_ld16(tO + 16u * c, o);
-                tmem_ld_wait16(o);
+        // columns 32h..32h+31 of S_t receive P[64h .. 64h+63] (two 32-column
+        // stores measured 0.4% faster than four of 16)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st16(tO + 16u * c, o);
-              }
-            }
-            l *= alpha;
-            m = m_new;
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            pk[k] = s[2 * h2][k];
+            pk[16 + k] = s[2 * h2 + 1][k];
           }
-          exp_pass(s, sc2, (m == -INFINITY) ? 0.f : m, lsum);
-        }
-        // columns 16c..16c+15 of S_t receive P[32c .. 32c+31]
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) pk[k] = s[c][k];
-          tmem_st16(tS + 16u * c, pk);
+          tmem_st32(tS + 32u * h2, pk);
         }
         {
           float a0, a1, b0, b1;
