@@ -257,6 +257,96 @@ WS_API ws_status ws_fm_euler_cfg_step(void* z, ws_dtype z_dt, const void* v_unco
                                       ws_stream_t stream);
 
 /*
+ * Device-resident unit sizes, for a unit step captured once in a CUDA graph
+ * and replayed unit after unit.  [youleyou] 3.3 (the performer's path runs
+ * under CUDA Graph capture), [explainer] "点开看部署细节" and [close-read]
+ * 四、推理, closing paragraph (CUDA graph capture keeps the per-unit path
+ * within its 160 ms budget).  A graph replays fixed launches with fixed
+ * arguments, so the sizes that change from unit to unit (the cache length,
+ * the ragged unit size) live in device memory, where the kernels read them
+ * at run time and a small kernel advances them.
+ *
+ * ws_unit_state lives in device memory (24 bytes, 8-byte aligned), owned by
+ * the caller:
+ *   cache_len  cache rows (per head) holding the earlier units
+ *   n_new      tokens of the current unit (its slice, queries and cache rows
+ *              [cache_len, cache_len + n_new))
+ *   unit       index of the current unit in the caller's list of unit sizes
+ */
+typedef struct ws_unit_state {
+  int64_t cache_len;
+  int64_t n_new;
+  int64_t unit;
+} ws_unit_state;
+
+/*
+ * ws_kv_append_dev -- ws_kv_append with cache_len and n_new read from the
+ * device-resident state when the kernel runs.  The launch covers n_max
+ * tokens (the largest unit); tokens past n_new do nothing.
+ * k_new, v_new  device [n_max][num_heads][head_dim] (rows past n_new unread)
+ * d_state       device ws_unit_state
+ * A state with n_new outside [0, n_max] or cache_len + n_new outside
+ * [0, capacity] writes nothing and sets the device error word, which
+ * ws_get_device_error() reports as WS_ERR_CAPACITY.  Other errors as
+ * ws_kv_append, checked on the host.
+ */
+WS_API ws_status ws_kv_append_dev(const void* k_new, const void* v_new, void* k_cache,
+                                  void* v_cache, const ws_unit_state* d_state, int64_t n_max,
+                                  int64_t capacity, int num_heads, int head_dim, ws_dtype dt,
+                                  ws_stream_t stream);
+
+/*
+ * ws_block_causal_attn_dev -- ws_block_causal_attn of the current unit, its
+ * sizes read from the device-resident state when the kernels run: the query
+ * block is the unit's n_new tokens and every query row sees the keys
+ * j < kv_len = cache_len + n_new (the unit itself included: append first).
+ * The launch is sized for q_max query rows and the whole cache.
+ *
+ * q             device [q_max][num_heads][head_dim]; rows past n_new are read
+ *               and their results dropped, but they must hold finite values
+ *               (zero the buffer once; rows left from earlier units are fine):
+ *               a row of infinities or NaNs sends its warp to the slow exact
+ *               path of the softmax on every key tile
+ * out           device [q_max][num_heads][head_dim]; rows < n_new are written
+ * lse_or_null   device float32 [num_heads][q_max] (row stride q_max), or NULL
+ * d_state       device ws_unit_state
+ * k_cache,
+ * v_cache       device [num_heads][capacity][head_dim].  Cache rows from
+ *               cache_len + n_new up to the next multiple of 128 are read and
+ *               masked: V rows there must hold finite values (zero the caches
+ *               once when allocating them).
+ * workspace     device scratch of at least
+ *               ws_block_causal_attn_dev_workspace_size(q_max, capacity,
+ *               num_heads, head_dim) bytes (always needed: any unit's key range
+ *               may be split); contents on entry do not matter.
+ * Implemented for WS_BF16 with head_dim 128 (else WS_ERR_UNSUPPORTED).  A
+ * state out of range (n_new outside [0, q_max], cache_len + n_new outside
+ * [0, capacity]) writes nothing and sets the device error word
+ * (WS_ERR_CAPACITY from ws_get_device_error); n_new == 0 does nothing.
+ */
+WS_API ws_status ws_block_causal_attn_dev(const void* q, const void* k_cache, const void* v_cache,
+                                          void* out, float* lse_or_null,
+                                          const ws_unit_state* d_state, int64_t q_max,
+                                          int64_t capacity, int num_heads, int head_dim,
+                                          float softmax_scale, ws_dtype dt, void* workspace,
+                                          size_t workspace_bytes, ws_stream_t stream);
+
+/* Workspace bytes for ws_block_causal_attn_dev on the current device
+ * (SIZE_MAX for invalid sizes). */
+WS_API size_t ws_block_causal_attn_dev_workspace_size(int64_t q_max, int64_t capacity,
+                                                      int num_heads, int head_dim);
+
+/*
+ * ws_unit_state_advance -- moves the device-resident state to the next unit
+ * (one thread, on the stream): cache_len += n_new; unit += 1; n_new =
+ * d_sizes[unit] if unit < n_sizes, else 0.
+ * d_sizes  device int32 [n_sizes], the sizes of the caller's units in order
+ * (may be NULL when n_sizes is 0).
+ */
+WS_API ws_status ws_unit_state_advance(ws_unit_state* d_state, const int32_t* d_sizes,
+                                       int64_t n_sizes, ws_stream_t stream);
+
+/*
  * Bytes of workspace ws_block_causal_attn (and ws_block_causal_attn_side)
  * needs for these sizes on the current device (0 when no key range is
  * split).  Returns SIZE_MAX when the
@@ -272,10 +362,13 @@ WS_API const char* ws_status_string(ws_status s);
 WS_API const char* ws_last_error(void);
 
 /*
- * Device error word written by the attention kernels when a bounded wait
- * gives up (they then stop, release their tensor memory and return).
- * Synchronises the current device.  *code_out = 0 when clean; otherwise the
- * call returns WS_ERR_TIMEOUT and *info_out says where: (wait site << 16) |
+ * Device error word written by the kernels.  Synchronises the current
+ * device.  *code_out = 0 when clean.  Code 2: a kernel with device-resident
+ * unit sizes found them out of range and wrote nothing; the call returns
+ * WS_ERR_CAPACITY, *info_out = 1 (n_new outside the launch's maximum) or 2
+ * (cache_len + n_new outside the capacity).  Code 1: an attention kernel's
+ * bounded wait gave up (it then stopped, released its tensor memory and
+ * returned); the call returns WS_ERR_TIMEOUT and *info_out says where: (wait site << 16) |
  * (block index & 0xFFFF), the first wait to give up.  Wait sites: 1 producer
  * waiting for the Q slot, 2 producer waiting for a K/V slot, 3 MMA issuer
  * waiting for Q, 4 MMA issuer waiting for a K/V tile, 5 MMA issuer waiting

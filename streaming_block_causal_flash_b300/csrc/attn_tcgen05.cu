@@ -88,8 +88,8 @@ constexpr int NUM_THREADS = 384;
 // the producer/MMA warpgroup shrinks to REGS_OTHER.  The sum must fit in what
 // the block is launched with (NUM_THREADS x the kernel's register count); the
 // host checks that before every launch.
-constexpr int REGS_SOFTMAX = 216;
-constexpr int REGS_OTHER = 72;
+constexpr int REGS_SOFTMAX = 208;
+constexpr int REGS_OTHER = 80;
 constexpr int REGS_NEEDED = 256 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -117,7 +117,8 @@ constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = 2 * TILE_BYTES;
 constexpr int SMEM_BARS = SMEM_KV + NSTAGE * TILE_BYTES;
 constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_MISC + 16;   // tmem slot, abort flag, issue lock, loads issued
+// tmem slot, abort flag, issue lock, loads issued; then the launch's sizes
+constexpr int SMEM_USED = SMEM_MISC + 16 + 32;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 // wait sites (error info)
@@ -151,7 +152,54 @@ struct Params {
   float* ws_lse;   // [grid*2][256]
   unsigned long long timeout_ns;
   int force_stall;   // test hook: one MMA issuer waits on a barrier nothing completes
+  // Device-resident unit sizes (unit mode only): when set, the unit's sizes
+  // are read at run time from dev_state = {cache_len, n_new} (the cache holds
+  // cache_len rows of earlier units and the n_new rows of the current one),
+  // and the launch was sized for at most q_max query rows and capacity keys.
+  const long long* dev_state;
+  int q_max;
 };
+
+// The sizes one launch works on: from the host plan, or from the
+// device-resident unit state.
+struct Dims {
+  int q_len;       // query rows
+  int kv_len;      // keys every row sees (unit mode)
+  int kv_tiles;    // ceil(kv_len / BN)
+  int groups;      // unit mode: CTA groups that have work (the others idle)
+  int lse_stride;  // row stride of the [H][rows] LSE output
+  long long work;  // unit mode: heads * kv_tiles
+};
+
+// Reads the sizes of this launch.  Returns false (every thread of every CTA
+// alike) when the launch has nothing to do; a device-resident state that is
+// out of range sets the device error word (code 2) and does nothing.
+__device__ __forceinline__ bool load_dims(const Params& P, Dims& D) {
+  if (P.dev_state == nullptr) {
+    D.q_len = P.q_len;
+    D.kv_len = P.kv_len;
+    D.kv_tiles = P.kv_tiles;
+    D.groups = P.groups;
+    D.lse_stride = P.q_len;
+    D.work = P.work;
+    return true;
+  }
+  const long long cache_len = P.dev_state[0];
+  const long long n_new = P.dev_state[1];
+  if (cache_len < 0 || n_new < 0 || n_new > P.q_max || cache_len > P.capacity - n_new) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && atomicCAS(&g_attn_error[0], 0u, 2u) == 0u)
+      g_attn_error[1] = static_cast<unsigned>(n_new > P.q_max || n_new < 0 ? 1 : 2);
+    return false;
+  }
+  if (n_new == 0) return false;
+  D.q_len = static_cast<int>(n_new);
+  D.kv_len = static_cast<int>(cache_len + n_new);
+  D.kv_tiles = (D.kv_len + BN - 1) / BN;
+  D.work = static_cast<long long>(P.heads) * D.kv_tiles;
+  D.groups = static_cast<int>(D.work < P.groups ? D.work : P.groups);
+  D.lse_stride = P.q_max;
+  return true;
+}
 
 struct Item {
   int h, pair, t0;
@@ -174,32 +222,38 @@ __device__ __forceinline__ int row_limit_dev(const int32_t* offs, int n_blocks, 
   return __ldg(offs + lo + 1);
 }
 
-__device__ __forceinline__ void iter_init(const Params& P, ItemIter& it) {
+__device__ __forceinline__ void iter_init(const Params& P, const Dims& D, ItemIter& it) {
   if (!P.prefill) {
     const int g = blockIdx.x / P.pairs;
     it.p = blockIdx.x % P.pairs;
-    it.fb = static_cast<long long>(g) * P.work / P.groups;
-    it.fe = static_cast<long long>(g + 1) * P.work / P.groups;
+    if (g < D.groups && 2 * it.p * BM < D.q_len) {
+      it.fb = static_cast<long long>(g) * D.work / D.groups;
+      it.fe = static_cast<long long>(g + 1) * D.work / D.groups;
+    } else {
+      // a group beyond the work, or a query-tile pair past the unit's rows
+      // (device-resident sizes, launch sized for a larger unit): idle
+      it.fb = it.fe = D.work;
+    }
     it.f = it.fb;
   } else {
     it.i = blockIdx.x;
   }
 }
 
-__device__ __forceinline__ bool iter_next(const Params& P, ItemIter& it, Item& item) {
+__device__ __forceinline__ bool iter_next(const Params& P, const Dims& D, ItemIter& it, Item& item) {
   if (!P.prefill) {
     if (it.f >= it.fe) return false;
-    const int h = static_cast<int>(it.f / P.kv_tiles);
-    const int t0 = static_cast<int>(it.f % P.kv_tiles);
+    const int h = static_cast<int>(it.f / D.kv_tiles);
+    const int t0 = static_cast<int>(it.f % D.kv_tiles);
     const long long rem = it.fe - it.f;
-    const int t1 = static_cast<int>(rem < P.kv_tiles - t0 ? t0 + rem : P.kv_tiles);
+    const int t1 = static_cast<int>(rem < D.kv_tiles - t0 ? t0 + rem : D.kv_tiles);
     item.h = h;
     item.pair = it.p;
     item.t0 = t0;
-    item.slot = (t0 == 0 && t1 == P.kv_tiles) ? -1
-                                              : (h == static_cast<int>(it.fb / P.kv_tiles) ? 0 : 1);
+    item.slot = (t0 == 0 && t1 == D.kv_tiles) ? -1
+                                              : (h == static_cast<int>(it.fb / D.kv_tiles) ? 0 : 1);
     for (int t = 0; t < 2; ++t)
-      item.n[t] = ((2 * it.p + t) * BM < P.q_len) ? (t1 - t0) : 0;
+      item.n[t] = ((2 * it.p + t) * BM < D.q_len) ? (t1 - t0) : 0;
     it.f += t1 - t0;
     return true;
   }
@@ -210,8 +264,8 @@ __device__ __forceinline__ bool iter_next(const Params& P, ItemIter& it, Item& i
   item.slot = -1;
   for (int t = 0; t < 2; ++t) {
     const int r0 = (2 * item.pair + t) * BM;
-    if (r0 < P.q_len) {
-      const int last = min(r0 + BM, P.q_len) - 1;
+    if (r0 < D.q_len) {
+      const int last = min(r0 + BM, D.q_len) - 1;
       const int e = row_limit_dev(P.offs, P.n_blocks, P.q_row0 + last);
       item.n[t] = (e + BN - 1) / BN;
     } else {
@@ -340,6 +394,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_ks,
                     const __grid_constant__ CUtensorMap tm_vs, const Params P) {
+  // Sizes of this launch; with device-resident sizes every thread reads the
+  // same state, so a launch with nothing to do returns in every thread.
+  Dims dims;
+  if (!load_dims(P, dims)) return;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -352,6 +410,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   int* issue_lk = reinterpret_cast<int*>(sgen + SMEM_MISC + 8);
   // K/V tile loads the producer has issued so far (paces the commit copy)
   volatile int* loads_issued = reinterpret_cast<volatile int*>(sgen + SMEM_MISC + 12);
+  // the launch's sizes, kept in shared memory (read at item boundaries only,
+  // so that they hold no registers through the hot loops)
+  Dims* sdims = reinterpret_cast<Dims*>(sgen + SMEM_MISC + 16);
   auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x >> 5;
@@ -377,6 +438,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     *abort_flag = 0;
     *issue_lk = 0;
     *loads_issued = 0;
+    *sdims = dims;
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -387,6 +449,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const Dims& D = *sdims;
   // Each role's code sits inside the branch that sets its register budget,
   // so the compiler allocates every region against the right limit.
   if (warp >= 8) {
@@ -402,13 +465,13 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         tma_prefetch_map(&tm_vs);
       }
       ItemIter it;
-      iter_init(P, it);
+      iter_init(P, D, it);
       Item item;
       Ring ring;
       uint32_t q_phase = 0;
       int issued = 0, q_issued = 0;
       bool ok = true;
-      while (ok && iter_next(P, it, item)) {
+      while (ok && iter_next(P, D, it, item)) {
         if (!wait_bar(bar(BAR_Q_EMPTY), q_phase ^ 1u, abort_flag, P.timeout_ns, W_PROD_QE)) break;
         q_phase ^= 1u;
         ++q_issued;
@@ -483,7 +546,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t tS = tmem + 256u * t;
       const uint32_t tO = tS + 128u;
       ItemIter it;
-      iter_init(P, it);
+      iter_init(P, D, it);
       Item item;
       Ring ring;
       uint32_t q_phase = 0, p_phase = 0, of_phase = 0;
@@ -513,7 +576,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         wait_bar(bar(BAR_STALL), 0u, abort_flag, P.timeout_ns, W_FORCED);
         ok = false;
       }
-      while (ok && iter_next(P, it, item)) {
+      while (ok && iter_next(P, D, it, item)) {
         const int n_iter = max(item.n[0], item.n[1]);
         const int n = item.n[t];
         if (!wait_bar(bar(BAR_Q_FULL), q_phase, abort_flag, P.timeout_ns, W_MMA_Q)) break;
@@ -612,7 +675,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       uint4* k_dst = reinterpret_cast<uint4*>(P.k_cache);
       uint4* v_dst = reinterpret_cast<uint4*>(P.v_cache);
       ItemIter it;
-      iter_init(P, it);
+      iter_init(P, D, it);
       const long long my_loads = 2 * (it.fe - it.fb);           // unit mode: K and V per key tile
       const long long iters = (r_end - r_begin + 2 * ROWS - 1) / (2 * ROWS);
       const long long head = my_loads < NSTAGE ? my_loads : NSTAGE;
@@ -673,16 +736,16 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tO = tS + 128u;
     uint32_t s_phase = 0, o_phase = 0;
     ItemIter it;
-    iter_init(P, it);
+    iter_init(P, D, it);
     Item item;
     bool ok = true;
-    while (ok && iter_next(P, it, item)) {
+    while (ok && iter_next(P, D, it, item)) {
       const int n = item.n[t];
       if (n == 0) continue;
       const int row = (2 * item.pair + t) * BM + r_in_tile;   // local query row
-      const bool valid = row < P.q_len;
+      const bool valid = row < D.q_len;
       const int e_row = (P.prefill && valid) ? row_limit_dev(P.offs, P.n_blocks, P.q_row0 + row)
-                                             : P.kv_len;
+                                             : D.kv_len;
       float m = -INFINITY, l = 0.f;
       for (int jj = 0; jj < n; ++jj) {
         const bool got = wait_bar(bar(BAR_S_FULL + t), s_phase, abort_flag, P.timeout_ns, W_SM_S);
@@ -813,7 +876,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
         if (valid && P.lse != nullptr)
-          P.lse[static_cast<size_t>(item.h) * P.q_len + row] = lse2 * LN2;
+          P.lse[static_cast<size_t>(item.h) * D.lse_stride + row] = lse2 * LN2;
       } else {
         const size_t slot = static_cast<size_t>(blockIdx.x) * 2 + item.slot;
         const size_t prow = slot * 256 + t * BM + r_in_tile;
@@ -872,17 +935,19 @@ constexpr int COMBINE_MAX_GROUPS = 1024;
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(Params P) {
   __shared__ int s_gs[COMBINE_MAX_GROUPS];
+  Dims D;
+  if (!load_dims(P, D)) return;
   const int h = blockIdx.y;
-  const long long L = P.kv_tiles;
-  const int g_lo = group_of(h * L, P.work, P.groups);
-  const int g_hi = group_of((h + 1) * L - 1, P.work, P.groups);
+  const long long L = D.kv_tiles;
+  const int g_lo = group_of(h * L, D.work, D.groups);
+  const int g_hi = group_of((h + 1) * L - 1, D.work, D.groups);
   if (g_lo == g_hi) return;   // one group covered the head: final output already written
   const int cnt = g_hi - g_lo + 1;
   // slot index (partial row block) of group g: (g * pairs + pair) * 2 + slot,
   // stored without the pair term, which depends on the row
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
     const int g = g_lo + i;
-    const int slot = (h == static_cast<int>(group_begin(g, P.work, P.groups) / L)) ? 0 : 1;
+    const int slot = (h == static_cast<int>(group_begin(g, D.work, D.groups) / L)) ? 0 : 1;
     s_gs[i] = g * 2 * P.pairs + slot;
   }
   __syncthreads();
@@ -912,7 +977,7 @@ attn_combine_kernel(Params P) {
       for (int u = 0; u < CB; ++u) {
         l[k][u] = -INFINITY;
         o[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row < P.q_len && i0 + u < cnt) {
+        if (row < D.q_len && i0 + u < cnt) {
           const size_t prow = static_cast<size_t>(s_gs[i0 + u] + 2 * (row >> 8)) * 256 + (row & 255);
           l[k][u] = ws_lse[prow];
           o[k][u] = reinterpret_cast<const float4*>(ws_o + prow * HD)[lane];
@@ -942,14 +1007,14 @@ attn_combine_kernel(Params P) {
 #pragma unroll
   for (int k = 0; k < RW; ++k) {
     const int row = row0 + k;
-    if (row >= P.q_len) break;
+    if (row >= D.q_len) break;
     const float inv = 1.f / sum[k];
     uint2 packed;
     packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
     packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
     reinterpret_cast<uint2*>(P.out + (static_cast<size_t>(row) * P.heads + h) * HD)[lane] = packed;
     if (lane == 0 && P.lse != nullptr)
-      P.lse[static_cast<size_t>(h) * P.q_len + row] = (m[k] + log2f(sum[k])) * LN2;
+      P.lse[static_cast<size_t>(h) * D.lse_stride + row] = (m[k] + log2f(sum[k])) * LN2;
   }
 }
 
@@ -1005,6 +1070,11 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
   }
   p.workspace_bytes = p.split ? static_cast<size_t>(p.grid) * 2 * 256 * (HD + 1) * sizeof(float) : 0;
   return true;
+}
+
+void plan_force_split(TcAttnPlan& p) {
+  p.split = true;
+  p.workspace_bytes = static_cast<size_t>(p.grid) * 2 * 256 * (HD + 1) * sizeof(float);
 }
 
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
@@ -1066,6 +1136,10 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   }
   P.timeout_ns = timeout_ns;
   P.force_stall = a.force_stall;
+  // device-resident sizes: the plan was made for the largest unit (q_len =
+  // q_max) and the whole cache (kv_len = capacity)
+  P.dev_state = a.dev_state;
+  P.q_max = plan.q_len;
   attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs, P);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

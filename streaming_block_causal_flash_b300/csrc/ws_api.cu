@@ -243,6 +243,17 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   return ok();
 }
 
+// Bytes of split-KV workspace for a launch sized by the device-resident
+// variant (largest unit q_max, whole cache), or 0 when the plan fails.
+size_t dev_workspace_bytes(int64_t q_max, int64_t capacity, int num_heads, int sms) {
+  ws::TcAttnPlan plan;
+  if (!ws::plan_tc_attn(plan, false, num_heads, (int)q_max, (int)(capacity - q_max), (int)capacity,
+                        1, sms))
+    return 0;
+  ws::plan_force_split(plan);
+  return plan.workspace_bytes;
+}
+
 }  // namespace
 
 namespace ws {
@@ -255,7 +266,7 @@ ws_status record_failure(ws_status s, const char* msg) { return fail(s, "%s", ms
 
 extern "C" {
 
-int ws_abi_version(void) { return 100; }
+int ws_abi_version(void) { return 101; }
 
 const char* ws_status_string(ws_status s) {
   switch (s) {
@@ -407,20 +418,150 @@ size_t ws_block_causal_attn_workspace_size(int64_t q_len, int64_t kv_len, int nu
   return need;
 }
 
+ws_status ws_kv_append_dev(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           const ws_unit_state* d_state, int64_t n_max, int64_t capacity,
+                           int num_heads, int head_dim, ws_dtype dt, ws_stream_t stream) {
+  const char* who = "ws_kv_append_dev";
+  if (!valid_dtype(dt)) return fail(WS_ERR_INVALID_ARGUMENT, "%s: unknown dtype", who);
+  if (n_max < 1 || capacity < n_max || num_heads < 1 || head_dim < 1)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: need 1 <= n_max <= capacity, heads and head_dim >= 1",
+                who);
+  const int64_t row_bytes = (int64_t)head_dim * (int64_t)dtype_size(dt);
+  if (row_bytes % 16 != 0)
+    return fail(WS_ERR_UNSUPPORTED, "%s: head_dim*sizeof(dtype) must be a multiple of 16", who);
+  if ((int64_t)num_heads * row_bytes > (int64_t)INT32_MAX || n_max > (int64_t)INT32_MAX)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: slice too large", who);
+  if (!k_new || !v_new || !k_cache || !v_cache || !d_state)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer argument", who);
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(d_state) & 7u))
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: misaligned pointer", who);
+  cudaError_t e = ws::launch_kv_append_dev(k_new, v_new, k_cache, v_cache,
+                                           reinterpret_cast<const long long*>(d_state), n_max,
+                                           capacity, num_heads, (int)row_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  return ok();
+}
+
+size_t ws_block_causal_attn_dev_workspace_size(int64_t q_max, int64_t capacity, int num_heads,
+                                               int head_dim) {
+  if (q_max < 1 || capacity < q_max || capacity > INT32_MAX || num_heads < 1 || head_dim != 128)
+    return SIZE_MAX;
+  const int sms = device_sms(nullptr);
+  if (sms <= 0) return SIZE_MAX;
+  const size_t need = dev_workspace_bytes(q_max, capacity, num_heads, sms);
+  return need == 0 ? SIZE_MAX : need;
+}
+
+ws_status ws_block_causal_attn_dev(const void* q, const void* k_cache, const void* v_cache,
+                                   void* out, float* lse_or_null, const ws_unit_state* d_state,
+                                   int64_t q_max, int64_t capacity, int num_heads, int head_dim,
+                                   float softmax_scale, ws_dtype dt, void* workspace,
+                                   size_t workspace_bytes, ws_stream_t stream) {
+  const char* who = "ws_block_causal_attn_dev";
+  if (!valid_dtype(dt)) return fail(WS_ERR_INVALID_ARGUMENT, "%s: unknown dtype %d", who, (int)dt);
+  if (dt != WS_BF16 || head_dim != 128)
+    return fail(WS_ERR_UNSUPPORTED, "%s: implemented for bf16 with head_dim 128", who);
+  if (!q || !k_cache || !v_cache || !out || !d_state || !workspace)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer argument", who);
+  if (num_heads < 1 || (int64_t)num_heads * head_dim > 65535)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: num_heads out of range", who);
+  if (q_max < 1 || capacity < q_max || capacity > (int64_t)INT32_MAX)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: need 1 <= q_max <= capacity <= INT32_MAX", who);
+  if (!(softmax_scale >= 0.f) || !std::isfinite(softmax_scale))
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: softmax_scale must be finite and >= 0", who);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(d_state) & 7u) ||
+      (lse_or_null && (reinterpret_cast<uintptr_t>(lse_or_null) & 3u)))
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: misaligned pointer", who);
+  int dev = 0;
+  const int sms = device_sms(&dev);
+  if (sms <= 0) return fail(WS_ERR_CUDA, "%s: cannot query the current device", who);
+  ws::TcAttnPlan plan;
+  if (!ws::plan_tc_attn(plan, false, num_heads, (int)q_max, (int)(capacity - q_max), (int)capacity,
+                        1, sms))
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: sizes out of range", who);
+  ws::plan_force_split(plan);
+  if (workspace_bytes < plan.workspace_bytes)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: workspace of %zu bytes needed, %zu given", who,
+                plan.workspace_bytes, workspace_bytes);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)head_dim);
+  // Q as a 2-D [q_max][H*D] matrix (rows past the unit are read, never
+  // written back); K and V as 3-D [H][capacity][D] views of the whole cache
+  // (the kernels mask keys at the run-time length).
+  CUtensorMap tm_q, tm_k, tm_v;
+  const cuuint64_t D = (cuuint64_t)head_dim;
+  {
+    cuuint64_t dims[2] = {D * (cuuint64_t)num_heads, (cuuint64_t)q_max};
+    cuuint64_t strides[1] = {D * (cuuint64_t)num_heads * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (!encode_bf16(&tm_q, q, 2, dims, strides, box))
+      return fail(WS_ERR_CUDA, "%s: cannot encode the Q tensor map", who);
+  }
+  {
+    cuuint64_t dims[3] = {D, (cuuint64_t)capacity, (cuuint64_t)num_heads};
+    cuuint64_t strides[2] = {D * 2, (cuuint64_t)capacity * D * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    if (!encode_bf16(&tm_k, k_cache, 3, dims, strides, box) ||
+        !encode_bf16(&tm_v, v_cache, 3, dims, strides, box))
+      return fail(WS_ERR_CUDA, "%s: cannot encode the K/V tensor maps", who);
+  }
+  ws::TcAttnArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.out = out;
+  a.lse = lse_or_null;
+  a.offs = nullptr;
+  a.capacity = capacity;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.force_stall = g_force_stall.load(std::memory_order_relaxed);
+  a.dev_state = reinterpret_cast<const long long*>(d_state);
+  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_k, tm_v,
+                                          g_timeout_ns.load(std::memory_order_relaxed), stream);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  return ok();
+}
+
+ws_status ws_unit_state_advance(ws_unit_state* d_state, const int32_t* d_sizes, int64_t n_sizes,
+                                ws_stream_t stream) {
+  const char* who = "ws_unit_state_advance";
+  if (!d_state || (n_sizes > 0 && !d_sizes) || n_sizes < 0)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer or negative size", who);
+  if (reinterpret_cast<uintptr_t>(d_state) & 7u)
+    return fail(WS_ERR_INVALID_ARGUMENT, "%s: misaligned state", who);
+  cudaError_t e = ws::launch_unit_state_advance(reinterpret_cast<long long*>(d_state), d_sizes,
+                                                n_sizes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  return ok();
+}
+
 ws_status ws_get_device_error(int* code_out, int* info_out) {
   if (!code_out || !info_out) return fail(WS_ERR_INVALID_ARGUMENT, "ws_get_device_error: null");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "ws_get_device_error");
   e = ws::read_attn_device_error(code_out, info_out);
   if (e != cudaSuccess) return cuda_fail(e, "ws_get_device_error");
-  if (*code_out != 0)
+  if (*code_out == 0) {
+    // the append and state kernels keep their own word
+    e = ws::read_unit_device_error(code_out, info_out);
+    if (e != cudaSuccess) return cuda_fail(e, "ws_get_device_error");
+  }
+  if (*code_out == 1)
     return fail(WS_ERR_TIMEOUT, "in-kernel wait gave up (site %d, block %d)", *info_out >> 16,
                 *info_out & 0xFFFF);
+  if (*code_out == 2)
+    return fail(WS_ERR_CAPACITY, "device-resident unit sizes out of range (%s); nothing was written",
+                *info_out == 1 ? "n_new outside [0, the launch's maximum]"
+                               : "cache_len + n_new outside [0, capacity]");
+  if (*code_out != 0) return fail(WS_ERR_CUDA, "unknown device error code %d", *code_out);
   return ok();
 }
 
 ws_status ws_clear_device_error(void) {
   cudaError_t e = ws::clear_attn_device_error();
+  if (e == cudaSuccess) e = ws::clear_unit_device_error();
   if (e != cudaSuccess) return cuda_fail(e, "ws_clear_device_error");
   return ok();
 }

@@ -17,6 +17,15 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
                              int64_t cache_len, int64_t n_new, int64_t capacity, int heads,
                              int row_bytes, int num_sms, cudaStream_t s);
 
+// Device-resident unit sizes (kv_append.cu): state = {cache_len, n_new, unit}.
+cudaError_t launch_kv_append_dev(const void* k_new, const void* v_new, void* k_cache,
+                                 void* v_cache, const long long* state, int64_t n_max,
+                                 int64_t capacity, int heads, int row_bytes, cudaStream_t s);
+cudaError_t launch_unit_state_advance(long long* state, const int32_t* sizes, int64_t n_sizes,
+                                      cudaStream_t s);
+cudaError_t read_unit_device_error(int* code, int* info);
+cudaError_t clear_unit_device_error();
+
 // ---- Flow-matching Euler step (fm_euler.cu)
 cudaError_t launch_fm_euler(float* z, const void* v, bool v_is_bf16, void* z_bf16_out,
                             int64_t n, float dtau, int num_sms, cudaStream_t s);
@@ -82,7 +91,15 @@ struct TcAttnArgs {
   int commit;            // side mode: also write the side K/V into the cache
   const void* k_side;    // side mode: the newest block's K/V, [q_len][H][128] (commit source)
   const void* v_side;
+  // Device-resident unit sizes {cache_len, n_new} (ws_unit_state), read by the
+  // kernels at run time; null for host-sized launches.  With it the plan
+  // must be made for q_len = the largest unit and kv_len = capacity, with
+  // split forced on (workspace and merge for any key range).
+  const long long* dev_state;
 };
+// Forces the split-KV merge and its workspace on (device-resident sizes,
+// where a launch can split any head's key range).
+void plan_force_split(TcAttnPlan& p);
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const CUtensorMap& tm_ks,

@@ -46,6 +46,11 @@ SIGNATURES = {
     "ws_fm_euler_step": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _c_i64, _c_f32, _vp]),
     "ws_fm_euler_cfg_step": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _vp, _c_i64, _c_f32, _c_f32, _vp]),
     "ws_block_causal_attn_workspace_size": (_c_size, [_c_i64, _c_i64, _c_int, _c_int]),
+    "ws_kv_append_dev": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int, _c_int, _vp]),
+    "ws_block_causal_attn_dev": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int,
+                                          _c_f32, _c_int, _vp, _c_size, _vp]),
+    "ws_block_causal_attn_dev_workspace_size": (_c_size, [_c_i64, _c_i64, _c_int, _c_int]),
+    "ws_unit_state_advance": (_c_int, [_vp, _vp, _c_i64, _vp]),
     "ws_status_string": (ctypes.c_char_p, [_c_int]),
     "ws_last_error": (ctypes.c_char_p, []),
     "ws_get_device_error": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
@@ -272,11 +277,82 @@ def ws_block_causal_attn_workspace_size(q_len: int, kv_len: int, num_heads: int,
     return int(n)
 
 
+# ---------------------------------------------- device-resident unit sizes
+
+def unit_state(cache_len: int, n_new: int, unit: int = 0, device="cuda") -> torch.Tensor:
+    """A ws_unit_state {cache_len, n_new, unit} in device memory (int64 [3])."""
+    return torch.tensor([int(cache_len), int(n_new), int(unit)], dtype=torch.int64, device=device)
+
+
+def _state_ptr(state: torch.Tensor) -> int:
+    if state.dtype != torch.int64 or state.numel() != 3:
+        raise ValueError("state must be an int64 tensor of 3 values (ws_unit_state)")
+    return _dev(state, "state")
+
+
+def ws_kv_append_dev(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                     v_cache: torch.Tensor, state: torch.Tensor, stream=None) -> None:
+    """ws_kv_append with cache_len / n_new read from the device state when the
+    kernel runs; the slices are buffers of n_max = k_new.shape[0] rows."""
+    n_max, H, D = k_new.shape
+    if tuple(v_new.shape) != (n_max, H, D):
+        raise ValueError("K and V slices differ in shape")
+    if k_cache.dim() != 3 or k_cache.shape[0] != H or k_cache.shape[2] != D or \
+            tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape must be [H, capacity, D] and match the slice")
+    dt = k_new.dtype
+    _check(load().ws_kv_append_dev(_dev(k_new, "k_new"), _dev(v_new, "v_new", dt),
+                                   _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
+                                   _state_ptr(state), int(n_max), int(k_cache.shape[1]), int(H), int(D),
+                                   _dtype_code(k_new), _stream_ptr(stream)))
+
+
+def ws_block_causal_attn_dev_workspace_size(q_max: int, capacity: int, num_heads: int,
+                                            head_dim: int) -> int:
+    n = load().ws_block_causal_attn_dev_workspace_size(int(q_max), int(capacity), int(num_heads),
+                                                       int(head_dim))
+    if n == ctypes.c_size_t(-1).value:
+        raise WsError(WS_ERR_INVALID_ARGUMENT, "workspace size query failed")
+    return int(n)
+
+
+def ws_block_causal_attn_dev(q, k_cache, v_cache, out, state: torch.Tensor,
+                             lse: Optional[torch.Tensor] = None, softmax_scale: float = 0.0,
+                             workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The current unit's queries (rows < n_new of a q_max-row buffer) against
+    the cache, sizes read from the device state when the kernels run."""
+    if k_cache.dim() != 3 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must both be [H, capacity, D]")
+    H, cap, D = k_cache.shape
+    if q.dim() != 3 or q.shape[1] != H or q.shape[2] != D or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q/out must be [q_max, H, D]")
+    q_max = int(q.shape[0])
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (H, q_max)):
+        raise ValueError("lse must be float32 [H, q_max]")
+    if workspace is None:
+        raise ValueError("ws_block_causal_attn_dev needs a workspace")
+    dt = q.dtype
+    _check(load().ws_block_causal_attn_dev(
+        _dev(q, "q"), _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt), _dev(out, "out", dt),
+        _dev(lse, "lse", torch.float32), _state_ptr(state), q_max, int(cap), int(H), int(D),
+        float(softmax_scale), _dtype_code(q), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+
+
+def ws_unit_state_advance(state: torch.Tensor, sizes_dev: torch.Tensor, stream=None) -> None:
+    """cache_len += n_new; unit += 1; n_new = sizes[unit] (0 past the end)."""
+    if sizes_dev.dtype != torch.int32 or sizes_dev.dim() != 1:
+        raise ValueError("sizes must be a 1-D int32 device tensor")
+    _check(load().ws_unit_state_advance(_state_ptr(state), _dev(sizes_dev, "sizes"),
+                                        int(sizes_dev.numel()), _stream_ptr(stream)))
+
+
 def ws_get_device_error():
-    """(code, info) of the attention kernels' device error word (synchronises)."""
+    """(code, info) of the kernels' device error word (synchronises): code 1 a
+    wait time-out, code 2 device-resident unit sizes out of range."""
     code, info = ctypes.c_int(0), ctypes.c_int(0)
     st = load().ws_get_device_error(ctypes.byref(code), ctypes.byref(info))
-    if st not in (WS_OK, WS_ERR_TIMEOUT):
+    if st not in (WS_OK, WS_ERR_TIMEOUT, WS_ERR_CAPACITY):
         _check(st)
     return code.value, info.value
 

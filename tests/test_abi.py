@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert lib.ws_status_string(0) == b"WS_OK"
     assert lib.ws_status_string(5) == b"WS_ERR_TIMEOUT"
-    assert ws.ws_abi_version() == 100
+    assert ws.ws_abi_version() == 101
 
 
 FAKE = 0x10000          # 16-byte aligned, never dereferenced by host validation
@@ -240,3 +240,39 @@ def test_binding_rejects_shapes_the_abi_cannot_see():
     full = torch.zeros(60, H, D, dtype=bf)
     with pytest.raises(ValueError, match="CUDA tensor"):
         ws.ws_block_causal_prefill(full, k, k, torch.empty_like(full), offs, offs_dev)
+
+
+def test_device_resident_entry_points_host_validation(lib):
+    """The device-resident-size variants check on the host everything that
+    does not depend on the sizes the kernels read at run time."""
+    # append: n_max above capacity, unsupported row size, null state, misaligned state
+    assert lib.ws_kv_append_dev(FAKE, FAKE, FAKE, FAKE, FAKE, 20, 10, 2, 128, ws.WS_BF16, None) \
+        == ws.WS_ERR_INVALID_ARGUMENT
+    assert lib.ws_kv_append_dev(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 2, 4, ws.WS_BF16, None) \
+        == ws.WS_ERR_UNSUPPORTED
+    assert lib.ws_kv_append_dev(FAKE, FAKE, FAKE, FAKE, None, 4, 10, 2, 128, ws.WS_BF16, None) \
+        == ws.WS_ERR_INVALID_ARGUMENT
+    assert lib.ws_kv_append_dev(FAKE, FAKE, FAKE, FAKE, FAKE + 4, 4, 10, 2, 128, ws.WS_BF16, None) \
+        == ws.WS_ERR_INVALID_ARGUMENT
+    # attention: only bf16 with head_dim 128; q_max within capacity; workspace required
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, st=FAKE, q_max=300, cap=1000, h=2, d=128,
+                scale=0.0, dt=ws.WS_BF16, wsp=FAKE, wsb=1 << 30)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.ws_block_causal_attn_dev(a["q"], a["k"], a["v"], a["o"], a["lse"], a["st"], a["q_max"],
+                                            a["cap"], a["h"], a["d"], a["scale"], a["dt"], a["wsp"],
+                                            a["wsb"], None)
+    assert call(dt=ws.WS_F32) == ws.WS_ERR_UNSUPPORTED
+    assert call(d=64) == ws.WS_ERR_UNSUPPORTED
+    assert call(q_max=2000) == ws.WS_ERR_INVALID_ARGUMENT
+    assert call(q_max=0) == ws.WS_ERR_INVALID_ARGUMENT
+    assert call(wsp=None) == ws.WS_ERR_INVALID_ARGUMENT
+    assert call(st=None) == ws.WS_ERR_INVALID_ARGUMENT
+    assert call(scale=-1.0) == ws.WS_ERR_INVALID_ARGUMENT
+    assert call(q=FAKE + 8) == ws.WS_ERR_INVALID_ARGUMENT
+    assert lib.ws_block_causal_attn_dev_workspace_size(0, 10, 2, 128) == ctypes.c_size_t(-1).value
+    assert lib.ws_block_causal_attn_dev_workspace_size(20, 10, 2, 128) == ctypes.c_size_t(-1).value
+    # state advance: null state, negative size count
+    assert lib.ws_unit_state_advance(None, FAKE, 3, None) == ws.WS_ERR_INVALID_ARGUMENT
+    assert lib.ws_unit_state_advance(FAKE, FAKE, -1, None) == ws.WS_ERR_INVALID_ARGUMENT
