@@ -2,7 +2,12 @@
 
 nvcc compiles every ``csrc/*.cu`` for sm_103a only and links them into one
 shared object with the CUDA runtime linked statically; the C ABI is
-``include/ws.h``.  Run as ``python -m streaming_block_causal_flash_b300.build``.
+``include/ws.h``.  ``build(debug=True)`` builds ``libws_b300_debug.so`` from
+the same sources with ``-DWS_DEBUG=1``: every index a kernel computes for a
+global-memory access is bounds-checked, and a failed check is recorded in the
+device error word and the access skipped (never a trap).  The binding loads
+the debug library when the environment variable ``WS_DEBUG=1`` is set.
+Run as ``python -m streaming_block_causal_flash_b300.build [--debug]``.
 """
 from __future__ import annotations
 
@@ -16,6 +21,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
 LIB_NAME = "libws_b300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libws_b300_debug.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,22 +36,24 @@ def sources():
     return sorted(glob.glob(os.path.join(PKG_DIR, "csrc", "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = sources() + glob.glob(os.path.join(PKG_DIR, "csrc", "*.h")) + \
         glob.glob(os.path.join(PKG_DIR, "csrc", "*.cuh")) + [os.path.join(ROOT, "include", "ws.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not force and not _stale(path):
+        return path
     cmd = [nvcc_path(), "-O3", "-std=c++17", *ARCH_FLAGS, "-lineinfo",
            "-Xcompiler", "-fPIC,-fvisibility=hidden", "-shared",
            "-I", os.path.join(ROOT, "include"),
-           "-o", LIB_PATH + ".tmp", *sources()]
+           *(["-DWS_DEBUG=1"] if debug else []),
+           "-o", path + ".tmp", *sources()]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))
@@ -54,10 +62,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
     if verbose:
         print(res.stdout + res.stderr)
-    os.replace(LIB_PATH + ".tmp", LIB_PATH)
-    return LIB_PATH
+    os.replace(path + ".tmp", path)
+    return path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB_PATH)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

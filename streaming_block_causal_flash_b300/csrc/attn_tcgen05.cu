@@ -67,12 +67,14 @@
 
 #include <mutex>
 
+#include "ws_debug.cuh"
 #include "ws_internal.h"
 #include "ws_ptx.cuh"
 
 namespace ws {
 
-// Device error word: [0] code (0 = clean, 1 = wait time-out), [1] info.
+// Device error word: [0] code (0 = clean, 1 = wait time-out, 2 = device-
+// resident sizes out of range, 3 = a debug-build bounds check failed), [1] info.
 __device__ unsigned int g_attn_error[2];
 
 namespace {
@@ -701,7 +703,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int u = 0; u < ROWS; ++u) {
           const long long r = r0 + u;
-          if (r < r_end)
+          if (r < r_end &&
+              WS_BOUND(g_attn_error, (r < per_tensor ? r : r - per_tensor) * CPR + col,
+                       per_tensor * CPR, 27))
             val[u] = ld_nc_na(r < per_tensor ? k_src + r * CPR + col
                                              : v_src + (r - per_tensor) * CPR + col);
         }
@@ -714,7 +718,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int u = 0; u < ROWS; ++u) {
           if (r0 + u < r_end) {
             uint4* dst = is_v ? v_dst : k_dst;
-            dst[(static_cast<long long>(h) * P.capacity + P.cache_len + t) * CPR + col] = val[u];
+            const long long at = (static_cast<long long>(h) * P.capacity + P.cache_len + t) * CPR + col;
+            if (WS_BOUND(g_attn_error, at, P.heads * P.capacity * CPR, 28)) dst[at] = val[u];
           }
           if (++h == P.heads) {
             h = 0;
@@ -857,12 +862,14 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float lse2 = m + __log2f(l);
       if (item.slot < 0) {
         __nv_bfloat16* dst = P.out + (static_cast<size_t>(row) * P.heads + item.h) * HD;
+        const bool put = valid && WS_BOUND(g_attn_error, (static_cast<long long>(row) * P.heads + item.h) * HD,
+                                           static_cast<long long>(D.lse_stride) * P.heads * HD, 21);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32u * c, o);
           tmem_ld_wait(o);
-          if (valid) {
+          if (put) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -875,18 +882,21 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
           }
         }
-        if (valid && P.lse != nullptr)
+        if (put && P.lse != nullptr &&
+            WS_BOUND(g_attn_error, static_cast<long long>(item.h) * D.lse_stride + row,
+                     static_cast<long long>(P.heads) * D.lse_stride, 22))
           P.lse[static_cast<size_t>(item.h) * D.lse_stride + row] = lse2 * LN2;
       } else {
         const size_t slot = static_cast<size_t>(blockIdx.x) * 2 + item.slot;
         const size_t prow = slot * 256 + t * BM + r_in_tile;
         float* dst = P.ws_o + prow * HD;
+        const bool put = valid && WS_BOUND(g_attn_error, prow, static_cast<long long>(gridDim.x) * 512, 23);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32u * c, o);
           tmem_ld_wait(o);
-          if (valid) {
+          if (put) {
             float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -894,7 +904,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                                   __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
           }
         }
-        if (valid) P.ws_lse[prow] = lse2;
+        if (put) P.ws_lse[prow] = lse2;
       }
       tc_fence_before();
       mbar_arrive(bar(BAR_O_FREE + t));
@@ -979,6 +989,7 @@ attn_combine_kernel(Params P) {
         o[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row < D.q_len && i0 + u < cnt) {
           const size_t prow = static_cast<size_t>(s_gs[i0 + u] + 2 * (row >> 8)) * 256 + (row & 255);
+          if (!WS_BOUND(g_attn_error, prow, static_cast<long long>(P.groups) * P.pairs * 512, 24)) continue;
           l[k][u] = ws_lse[prow];
           o[k][u] = reinterpret_cast<const float4*>(ws_o + prow * HD)[lane];
         }
@@ -1012,8 +1023,12 @@ attn_combine_kernel(Params P) {
     uint2 packed;
     packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
     packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
-    reinterpret_cast<uint2*>(P.out + (static_cast<size_t>(row) * P.heads + h) * HD)[lane] = packed;
-    if (lane == 0 && P.lse != nullptr)
+    if (WS_BOUND(g_attn_error, (static_cast<long long>(row) * P.heads + h) * HD,
+                 static_cast<long long>(D.lse_stride) * P.heads * HD, 25))
+      reinterpret_cast<uint2*>(P.out + (static_cast<size_t>(row) * P.heads + h) * HD)[lane] = packed;
+    if (lane == 0 && P.lse != nullptr &&
+        WS_BOUND(g_attn_error, static_cast<long long>(h) * D.lse_stride + row,
+                 static_cast<long long>(P.heads) * D.lse_stride, 26))
       P.lse[static_cast<size_t>(h) * D.lse_stride + row] = (m[k] + log2f(sum[k])) * LN2;
   }
 }

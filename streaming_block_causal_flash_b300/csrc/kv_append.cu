@@ -6,10 +6,17 @@
 // layout [H][capacity][row].  Pure data movement: every thread moves 16-byte
 // chunks, K and V in one launch (grid.y), several independent loads in
 // flight before the matching stores.
+#include "ws_debug.cuh"
 #include "ws_internal.h"
 
 namespace ws {
 namespace {
+
+// Device error word of this file's kernels: [0] code (0 clean, 2 device-
+// resident sizes out of range, 3 a debug-build bounds check failed), [1] info
+// (code 2: 1 n_new out of range, 2 the unit does not fit the capacity;
+// code 3: (check site << 16) | block).
+__device__ unsigned int g_unit_error[2];
 
 constexpr int kThreads = 128;
 constexpr int kMaxPerThread = 8;   // 16-byte chunks per thread held in flight
@@ -41,23 +48,22 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
 #pragma unroll
     for (int u = 0; u < kMaxPerThread; ++u) {
       const int c = base + u * kThreads;
-      if (c < per_token) val[u] = ld_stream(src + c);
+      if (c < per_token &&
+          WS_BOUND(g_unit_error, t * per_token + c, static_cast<int64_t>(gridDim.x) * per_token, 31))
+        val[u] = ld_stream(src + c);
     }
 #pragma unroll
     for (int u = 0; u < kMaxPerThread; ++u) {
       const int c = base + u * kThreads;
       if (c < per_token) {
         const int h = c / CH;
-        dst[h * head_stride + (c - h * CH)] = val[u];
+        const int64_t at = h * head_stride + (c - h * CH);
+        if (WS_BOUND(g_unit_error, (cache_len + t) * CH + at, heads * head_stride, 32))
+          dst[at] = val[u];
       }
     }
   }
 }
-
-// Device error word of the kernels with device-resident sizes: [0] code
-// (0 clean, 2 sizes out of range), [1] info (1: n_new out of range, 2: the
-// unit does not fit the capacity).
-__device__ unsigned int g_unit_error[2];
 
 __device__ __forceinline__ void unit_error(unsigned info) {
   if (atomicCAS(&g_unit_error[0], 0u, 2u) == 0u) g_unit_error[1] = info;
@@ -93,14 +99,18 @@ kv_append_dev_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ 
 #pragma unroll
     for (int u = 0; u < kMaxPerThread; ++u) {
       const int c = base + u * kThreads;
-      if (c < per_token) val[u] = ld_stream(src + c);
+      if (c < per_token &&
+          WS_BOUND(g_unit_error, t * per_token + c, static_cast<int64_t>(gridDim.x) * per_token, 31))
+        val[u] = ld_stream(src + c);
     }
 #pragma unroll
     for (int u = 0; u < kMaxPerThread; ++u) {
       const int c = base + u * kThreads;
       if (c < per_token) {
         const int h = c / CH;
-        dst[h * head_stride + (c - h * CH)] = val[u];
+        const int64_t at = h * head_stride + (c - h * CH);
+        if (WS_BOUND(g_unit_error, (cache_len + t) * CH + at, heads * head_stride, 32))
+          dst[at] = val[u];
       }
     }
   }

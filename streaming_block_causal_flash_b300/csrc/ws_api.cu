@@ -555,6 +555,10 @@ ws_status ws_get_device_error(int* code_out, int* info_out) {
     return fail(WS_ERR_CAPACITY, "device-resident unit sizes out of range (%s); nothing was written",
                 *info_out == 1 ? "n_new outside [0, the launch's maximum]"
                                : "cache_len + n_new outside [0, capacity]");
+  if (*code_out == 3)
+    return fail(WS_ERR_CUDA,
+                "debug build: an out-of-bounds access was caught and skipped (check site %d, block %d)",
+                *info_out >> 16, *info_out & 0xFFFF);
   if (*code_out != 0) return fail(WS_ERR_CUDA, "unknown device error code %d", *code_out);
   return ok();
 }

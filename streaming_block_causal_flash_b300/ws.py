@@ -16,7 +16,10 @@ import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libws_b300.so")
+# WS_DEBUG=1 selects the debug build (bounds-checked kernel indices; see
+# build.py), built with `python -m streaming_block_causal_flash_b300.build --debug`.
+LIB_PATH = os.path.join(_HERE, "libws_b300_debug.so" if os.environ.get("WS_DEBUG") == "1"
+                        else "libws_b300.so")
 
 WS_OK = 0
 WS_ERR_INVALID_ARGUMENT = 1

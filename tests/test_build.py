@@ -68,3 +68,15 @@ def test_attention_register_split_fits_the_launch(tmp_path):
     assert consts["NUM_THREADS"] == 384
     assert consts["REGS_SOFTMAX"] % 8 == 0 and consts["REGS_OTHER"] % 8 == 0
     assert need <= regs[0] * consts["NUM_THREADS"], f"split needs {need}, launch has {regs[0] * 384}"
+
+
+def test_debug_build_compiles_and_exports_every_symbol():
+    """The debug build (WS_DEBUG=1: bounds-checked kernel indices) compiles
+    for sm_103a from the same sources and exports the same C ABI."""
+    import ctypes
+    from tests.test_abi import declared_symbols
+    path = ws_build.build(debug=True)
+    assert path.endswith("libws_b300_debug.so")
+    lib = ctypes.CDLL(path)
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
