@@ -89,6 +89,29 @@ bool encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t*
   return r == CUDA_SUCCESS;
 }
 
+// Tensor maps for the TMA append (see ws::AppendMaps).  Returns false when the
+// sizes do not fit that path; the plain-copy kernel then runs instead.
+bool encode_append_maps(ws::AppendMaps& m, void* k_cache, void* v_cache, int heads,
+                        int64_t row_bytes, int64_t capacity) {
+  if (heads > ws::kTmaAppendMaxHeads || row_bytes > ws::kTmaAppendMaxRowBytes ||
+      heads * row_bytes > ws::kTmaAppendMaxTokenBytes || capacity > (int64_t)INT32_MAX)
+    return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)(row_bytes / 2), (cuuint64_t)heads, (cuuint64_t)capacity};
+  cuuint64_t strides[2] = {(cuuint64_t)capacity * (cuuint64_t)row_bytes, (cuuint64_t)row_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)(row_bytes / 2), (cuuint32_t)heads, 1};
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = fn(i == 0 ? &m.k : &m.v, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, i == 0 ? k_cache : v_cache,
+                    dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  return true;
+}
+
 // Shared validation for the two attention entry points.
 ws_status check_attn_args(const char* who, const void* q, const void* k_cache,
                           const void* v_cache, void* out, const float* lse,
@@ -313,10 +336,10 @@ ws_status ws_kv_append(const void* k_new, const void* v_new, void* k_cache, void
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: null pointer argument", who);
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: pointers must be 16-byte aligned", who);
-  const int sms = device_sms(nullptr);
-  if (sms <= 0) return fail(WS_ERR_CUDA, "%s: cannot query the current device", who);
+  ws::AppendMaps maps;
+  const bool tma = encode_append_maps(maps, k_cache, v_cache, num_heads, row_bytes, capacity);
   cudaError_t e = ws::launch_kv_append(k_new, v_new, k_cache, v_cache, cache_len, n_new, capacity,
-                                       num_heads, (int)row_bytes, sms, stream);
+                                       num_heads, (int)row_bytes, tma ? &maps : nullptr, stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
 }
@@ -436,9 +459,12 @@ ws_status ws_kv_append_dev(const void* k_new, const void* v_new, void* k_cache, 
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
       (reinterpret_cast<uintptr_t>(d_state) & 7u))
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: misaligned pointer", who);
+  ws::AppendMaps maps;
+  const bool tma = encode_append_maps(maps, k_cache, v_cache, num_heads, row_bytes, capacity);
   cudaError_t e = ws::launch_kv_append_dev(k_new, v_new, k_cache, v_cache,
                                            reinterpret_cast<const long long*>(d_state), n_max,
-                                           capacity, num_heads, (int)row_bytes, stream);
+                                           capacity, num_heads, (int)row_bytes,
+                                           tma ? &maps : nullptr, stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
 }

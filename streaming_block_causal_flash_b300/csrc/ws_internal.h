@@ -13,14 +13,29 @@ namespace ws {
 ws_status record_failure(ws_status s, const char* msg);
 
 // ---- KV append (kv_append.cu)
+// Tensor maps of the K and V caches for the TMA append: 16-bit elements,
+// dims (row_bytes / 2, heads, capacity) with byte strides (capacity *
+// row_bytes, row_bytes), box (row_bytes / 2, heads, 1), no swizzle.  Null
+// maps select the plain-load/store kernel (sizes the TMA path cannot take).
+struct AppendMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+// Largest slice row (all heads of one token) the TMA append stages in
+// shared memory, and the largest head count of its box.
+constexpr int kTmaAppendMaxTokenBytes = 200 * 1024;
+constexpr int kTmaAppendMaxHeads = 256;
+constexpr int kTmaAppendMaxRowBytes = 512;
+
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              int64_t cache_len, int64_t n_new, int64_t capacity, int heads,
-                             int row_bytes, int num_sms, cudaStream_t s);
+                             int row_bytes, const AppendMaps* maps, cudaStream_t s);
 
 // Device-resident unit sizes (kv_append.cu): state = {cache_len, n_new, unit}.
 cudaError_t launch_kv_append_dev(const void* k_new, const void* v_new, void* k_cache,
                                  void* v_cache, const long long* state, int64_t n_max,
-                                 int64_t capacity, int heads, int row_bytes, cudaStream_t s);
+                                 int64_t capacity, int heads, int row_bytes,
+                                 const AppendMaps* maps, cudaStream_t s);
 cudaError_t launch_unit_state_advance(long long* state, const int32_t* sizes, int64_t n_sizes,
                                       cudaStream_t s);
 cudaError_t read_unit_device_error(int* code, int* info);
