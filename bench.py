@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-hbm", action="store_true", help="skip the append/Euler HBM measurement")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the brief measurements of the other workloads (and the full oracle timings)")
     return ap.parse_args(argv)
 
 
@@ -790,6 +792,97 @@ def cpu_baseline(sess: UnitSession):
                       f"({flops / 1e9:.1f} GFLOP in {dt:.2f} s)"}
 
 
+def _timed(fn):
+    t0 = time.perf_counter()
+    out = fn()
+    return time.perf_counter() - t0, out
+
+
+def oracle_append_euler(sess: UnitSession, u: int):
+    """The oracle's full KV append of unit u's slice into the session's cache
+    (a bit copy; 16-bit views of the bf16 bytes) and its full Euler steps over
+    the unit's latents: seconds for each."""
+    from oracle import kv_cache as kc
+    k16 = sess.k_host.view(torch.int16).numpy()
+    v16 = sess.v_host.view(torch.int16).numpy()
+    kn, vn = (t.view(torch.int16).numpy() for t in sess.kv_host[u])
+    dt_app, _ = _timed(lambda: kc.kv_append(k16, v16, kn, vn, int(sess.offsets_all[u])))
+    return dt_app, oracle_step_rest(sess, u)
+
+
+def oracle_full(sess: UnitSession):
+    """The oracle timed in full where that takes seconds, on the machine's host
+    cores: every attention row of the tiny fp32 and 192x336 workloads, and the
+    append and Euler steps of the bench unit and the 192x336 unit.  The long
+    session's unit has the bench unit's shapes (its append copies a larger
+    cache; the oracle's append copies its whole cache, so its time scales
+    with the capacity) and the prefill's bulk append is timed on 8 of its 128
+    units -- both said so in the entries."""
+    from oracle import block_causal as bc
+    out = {}
+    # tiny fp32: the full prefill and the per-block incremental calls
+    w = WORKLOADS["tiny_fp32"]
+    offs = w.offsets()
+    k = torch.stack([w.head_timeline("k", 0, w.n_units)]).double().numpy()
+    v = torch.stack([w.head_timeline("v", 0, w.n_units)]).double().numpy()
+    q = w.head_timeline("q", 0, w.n_units).double().numpy()[:, None, :]
+    dt_p, _ = _timed(lambda: bc.block_causal_attention(q, k, v, offs))
+    dt_i, _ = _timed(lambda: [bc.unit_attention(q[int(offs[b]):int(offs[b + 1])], k[:, :int(offs[b + 1])],
+                                                 v[:, :int(offs[b + 1])], offs[:b + 2])
+                              for b in range(len(offs) - 1)])
+    out["tiny_fp32"] = {"prefill_s": round(dt_p, 4), "incremental_8_blocks_s": round(dt_i, 4)}
+    # 192x336: every row of the unit's attention, plus its append and Euler steps
+    s2 = UnitSession(WORKLOADS["unit_192x336"], None, host_only=True)
+    u2 = s2.units[0]
+    dt_a, fl, rows, heads = oracle_unit_sample(s2, u2, s2.sizes[u2])
+    dt_app2, dt_eu2 = oracle_append_euler(s2, u2)
+    out["unit_192x336"] = {"attention_s": round(dt_a, 3), "attention_tflops": round(fl / dt_a / 1e12, 6),
+                           "rows": rows, "heads": heads, "append_s": round(dt_app2, 4),
+                           "euler_4_steps_s": round(dt_eu2, 4)}
+    del s2
+    u = sess.units[0]
+    dt_app, dt_eu = oracle_append_euler(sess, u)
+    out[sess.w.name] = {"append_s": round(dt_app, 4), "euler_steps_s": round(dt_eu, 4),
+                        "cache_rows": int(sess.cap)}
+    out["long_session_640x368"] = {"note": f"same slice and latent shapes as {sess.w.name}: its Euler "
+                                           f"steps take the time above; its append copies a cache of "
+                                           f"{WORKLOADS['long_session_640x368'].capacity()} rows instead of "
+                                           f"{sess.cap}"}
+    # prefill: the bulk append of 8 units (all heads) into a cache of 8 units
+    wp = WORKLOADS["prefill_128x932"]
+    sizes = wp.unit_sizes()[:8]
+    kn = wp.token_major_range("k", 0, 8, sizes).view(torch.int16).numpy()
+    vn = wp.token_major_range("v", 0, 8, sizes).view(torch.int16).numpy()
+    from oracle import kv_cache as kc
+    cache = np.zeros((wp.heads, kn.shape[0], wp.head_dim), dtype=np.int16)
+    dt_b, _ = _timed(lambda: kc.kv_append(cache, cache, kn, vn, 0))
+    out["prefill_128x932"] = {"bulk_append_8_units_s": round(dt_b, 4),
+                              "extrapolated_128_units_s": round(dt_b * 16, 3),
+                              "note": "bulk append timed on 8 of the 128 units; the 128-unit figure is "
+                                      "that time x 16, an estimate"}
+    return out
+
+
+def prefill_cpu_baseline(w: Workload, q_h, k_h, v_h, offs, n_rows: int = 64, n_heads: int = 8):
+    """The oracle on a bounded sample of the prefill: n_rows evenly spaced
+    query rows x the first n_heads heads, each against its visible keys."""
+    from oracle import block_causal as bc
+    T = int(offs[-1])
+    rows = np.unique(np.linspace(0, T - 1, n_rows).astype(np.int64))
+    heads = list(range(min(n_heads, w.heads)))
+    e_max = int(offs[np.searchsorted(offs, rows.max(), side="right")])
+    k = k_h[:e_max, heads].transpose(0, 1).float().numpy()
+    v = v_h[:e_max, heads].transpose(0, 1).float().numpy()
+    q = q_h[rows][:, heads].float().numpy()
+    dt, _ = _timed(lambda: bc.attention_rows(q, rows, k, v, offs))
+    flops = attention_flops(offs, rows, len(heads), w.head_dim)
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            **host_cpu(),
+            "sample": f"fp64 numpy oracle, block-causal attention of {rows.size} evenly spaced query rows "
+                      f"x {len(heads)} heads of the {T}-token prefill against their visible keys "
+                      f"({flops / 1e9:.1f} GFLOP in {dt:.2f} s)"}
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
@@ -847,9 +940,22 @@ def workload_config(w: Workload, sess: UnitSession, u: int):
 # ------------------------------------------------------------ prefill arm
 
 def prefill_main(args, w: Workload, device, rank, world, peaks):
+    line = prefill_measure(args.steps, args.warmup, w, device, rank, world, peaks,
+                           with_e2e=not args.no_e2e,
+                           with_cpu=not args.no_cpu_baseline and world == 1 and rank == 0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world, device)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def prefill_measure(K: int, W: int, w: Workload, device, rank, world, peaks, with_e2e=True,
+                    with_cpu=False):
     """One step = the session prefill: bulk KV append of all T tokens, then
     full-sequence block-causal attention over them (every call through the C
-    ABI)."""
+    ABI).  Returns the bench line."""
     from streaming_block_causal_flash_b300 import ws
     sizes = w.unit_sizes()
     offs = w.offsets()
@@ -875,7 +981,6 @@ def prefill_main(args, w: Workload, device, rank, world, peaks):
         if ev is not None:
             ev[2].record(st)
 
-    K, W = args.steps, args.warmup
     for _ in range(W):
         step()
     torch.cuda.synchronize(device)
@@ -915,7 +1020,7 @@ def prefill_main(args, w: Workload, device, rank, world, peaks):
                          "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4)},
             "gpu_launches": 2 * K, "clocks": clk,
             "kernels_ms_mean": {"kv_append_bulk": round(append_ms, 4), "block_causal_prefill": round(attn_ms, 4)}}
-    if not args.no_e2e and rank == 0:
+    if with_e2e and rank == 0:
         hq, hk, hv = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
         ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         dq, dk, dv, do = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(out)
@@ -934,12 +1039,60 @@ def prefill_main(args, w: Workload, device, rank, world, peaks):
         line["e2e"] = {"value": round(flops / (e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                        "ms_per_step": round(e_ms, 3), "steps": reps,
                        "h2d_bytes_per_step": int(3 * q.numel() * 2), "d2h_bytes_per_step": int(out.numel() * 2)}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    barrier(world, device)
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    return 0
+    if with_cpu:
+        line["cpu_baseline"] = prefill_cpu_baseline(w, q_h, k_h, v_h, offs)
+    del q, k_new, v_new, kc, vc, out
+    return line
+
+
+def measure_unit_brief(name: str, device, peaks, steps: int = 10, warmup: int = 3):
+    """The unit step of another streaming workload, measured compactly so
+    that one bench line covers every configuration: per-step CUDA-event
+    times (each of the workload's new units in turn), the attention call's
+    TFLOP/s and roofline fraction, clocks, and the graph-replayed step."""
+    w = WORKLOADS[name]
+    sess = UnitSession(w, device)
+    n_units = len(sess.units)
+    K = max(steps, n_units)
+    args = argparse.Namespace(steps=K, warmup=min(warmup, K))
+    clocks = ClockSampler(device.index)
+    total_ms, flops, append_ms, attn_ms, euler_ms, unit_ms, clk = time_native(args, sess, device, 1, clocks)
+    per_attn = statistics.mean(sess.unit_flops(sess.units[i % n_units]) for i in range(K))
+    achieved = per_attn / (statistics.mean(attn_ms) * 1e-3) / 1e12
+    out = {"config": workload_config(w, sess, sess.units[0]), "steps": K,
+           "ms_per_step": round(total_ms / K, 4),
+           "value": round(flops / (total_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+           "per_unit_ms": {"mean": round(statistics.mean(unit_ms), 4),
+                           "p50": round(statistics.median(unit_ms), 4), "max": round(max(unit_ms), 4),
+                           "min": round(min(unit_ms), 4), "units": n_units},
+           "kernels_ms_mean": {"kv_append": round(statistics.mean(append_ms), 4),
+                               "block_causal_attn": round(statistics.mean(attn_ms), 4),
+                               "fm_euler_steps": round(statistics.mean(euler_ms), 4)},
+           "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)},
+           "clocks": clk}
+    if n_units == 1:
+        out["graph"] = time_unit_graph(sess, device)
+    del sess
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_other_workloads(device, peaks, exclude: str):
+    """Brief measurements of every bf16 workload but the line's own."""
+    res = {}
+    for name, w in WORKLOADS.items():
+        if w.dtype != "bf16" or name == exclude:
+            continue
+        if w.prefill:
+            line = prefill_measure(2, 1, w, device, 0, 1, peaks, with_e2e=False, with_cpu=True)
+            res[name] = {k: line[k] for k in ("config", "value", "unit", "ms_per_step", "roofline", "clocks",
+                                              "kernels_ms_mean", "cpu_baseline")}
+            res[name]["steps"] = 2
+        else:
+            res[name] = measure_unit_brief(name, device, peaks)
+        torch.cuda.empty_cache()
+    return res
 
 
 # --------------------------------------------------------------------- main
@@ -1029,6 +1182,10 @@ def main(argv=None):
             line["graph_fused_commit"] = time_fused_unit(sess, device)
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(sess)
+            if not args.no_other_workloads:
+                line["cpu_baseline"]["oracle_full"] = oracle_full(sess)
+        if not args.no_other_workloads and world == 1:
+            line["workloads"] = measure_other_workloads(device, peaks, w.name)
         print(json.dumps(line), flush=True)
     barrier(world, device)
     if world > 1:

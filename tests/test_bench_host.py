@@ -131,3 +131,21 @@ def test_clock_sampler_reads_nvml_snapshots_and_reasons(monkeypatch):
     assert 1900 <= out["sm_mhz"] <= 2000 and out["power_w_median"] == 900.0
     assert bench.clock_normalised(2.0, out) == round(2.0 * out["sm_mhz"], 1)
     assert bench.clock_normalised(2.0, {"sm_mhz": None}) is None
+
+
+def test_oracle_timing_suite_and_prefill_sample_on_the_cpu():
+    """The full oracle timings and the prefill's sampled oracle baseline run on
+    the host alone and report what they timed."""
+    from streaming_block_causal_flash_b300.inputs import Workload
+    sess = bench.UnitSession(bench.WORKLOADS["unit_192x336"], None, host_only=True)
+    full = bench.oracle_full(sess)
+    assert full["tiny_fp32"]["prefill_s"] > 0 and full["unit_192x336"]["rows"] == 264
+    assert full["unit_192x336"]["heads"] == 24 and full["unit_192x336"]["append_s"] > 0
+    assert "estimate" in full["prefill_128x932"]["note"]
+    w = Workload("p", seed=5, heads=2, head_dim=128, dtype="bf16", std=0.5, video_tokens=100,
+                 audio_tokens=0, text_tokens=0, history_units=0, new_units=6, latent_tokens=1,
+                 latent_channels=8, euler_steps=0, prefill=True)
+    sizes = w.unit_sizes()
+    q, k, v = (w.token_major_range(n, 0, w.n_units, sizes) for n in ("q", "k", "v"))
+    cb = bench.prefill_cpu_baseline(w, q, k, v, w.offsets(), n_rows=16, n_heads=2)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and "16 evenly spaced" in cb["sample"]
