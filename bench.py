@@ -842,8 +842,8 @@ def oracle_full(sess: UnitSession):
     del s2
     u = sess.units[0]
     dt_app, dt_eu = oracle_append_euler(sess, u)
-    out[sess.w.name] = {"append_s": round(dt_app, 4), "euler_steps_s": round(dt_eu, 4),
-                        "cache_rows": int(sess.cap)}
+    out.setdefault(sess.w.name, {}).update({"append_s": round(dt_app, 4), "euler_steps_s": round(dt_eu, 4),
+                                            "cache_rows": int(sess.cap)})
     out["long_session_640x368"] = {"note": f"same slice and latent shapes as {sess.w.name}: its Euler "
                                            f"steps take the time above; its append copies a cache of "
                                            f"{WORKLOADS['long_session_640x368'].capacity()} rows instead of "
