@@ -113,19 +113,23 @@ constexpr int BAR_O_FULL = BAR_P_FULL + 2;    // [2]
 constexpr int BAR_O_FREE = BAR_O_FULL + 2;    // [2]
 constexpr int BAR_DRAIN = BAR_O_FREE + 2;    // [2], one per MMA issuer
 constexpr int BAR_STALL = BAR_DRAIN + 2;      // never completed (test hook)
-constexpr int NUM_BARS = BAR_STALL + 1;
+constexpr int BAR_MERGE = BAR_STALL + 1;      // solo items: half 1's (m, l) are in shared memory
+constexpr int BAR_MERGE_FREE = BAR_MERGE + 1; // solo items: half 0 has read them
+constexpr int NUM_BARS = BAR_MERGE_FREE + 1;
 
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = 2 * TILE_BYTES;
 constexpr int SMEM_BARS = SMEM_KV + NSTAGE * TILE_BYTES;
 constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;
-// tmem slot, abort flag, issue lock, loads issued; then the launch's sizes
-constexpr int SMEM_USED = SMEM_MISC + 16 + 32;
+// tmem slot, abort flag, issue lock, loads issued; then the launch's sizes;
+// then a solo item's per-row (m, l) of TMEM half 1
+constexpr int SMEM_MERGE = SMEM_MISC + 16 + 32;
+constexpr int SMEM_USED = SMEM_MERGE + 2 * BM * 4;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 // wait sites (error info)
 enum : int { W_PROD_QE = 1, W_PROD_KVE, W_MMA_Q, W_MMA_KV, W_MMA_P, W_MMA_OF, W_SM_S, W_SM_O,
-             W_DRAIN_MMA, W_DRAIN_TMA, W_FORCED, W_LOCK, W_COMMIT };
+             W_DRAIN_MMA, W_DRAIN_TMA, W_FORCED, W_LOCK, W_COMMIT, W_SM_MERGE };
 
 struct Params {
   int prefill;
@@ -160,6 +164,14 @@ struct Params {
   // and the launch was sized for at most q_max query rows and capacity keys.
   const long long* dev_state;
   int q_max;
+  // Split-stream ("solo") CTAs, unit mode with host sizes: when the query
+  // block has an odd number of 128-row tiles, its last tile is not paired.
+  // It gets CTAs of its own: the first groups * pairs CTAs hold the full
+  // pairs as usual; the solo_groups CTAs after them each hold the last tile
+  // on both TMEM halves, which take alternate key tiles of the CTA's range
+  // and are merged in the epilogue.  Such a CTA runs its range at the rate of
+  // a paired CTA, so solo groups get twice the key range.
+  int solo, solo_groups;
 };
 
 // The sizes one launch works on: from the host plan, or from the
@@ -205,14 +217,46 @@ __device__ __forceinline__ bool load_dims(const Params& P, Dims& D) {
 
 struct Item {
   int h, pair, t0;
-  int n[2];        // key tiles for query tile 0 / 1 (0: tile has no rows)
+  int n[2];        // key tiles for query tile 0 / 1 (0: tile has no rows); for a solo
+                   // item, the key tiles of TMEM half 0 (even) and half 1 (odd)
   int slot;        // -1 final output, else partial slot 0/1
+  int solo;        // one query tile (2 * pair) on both halves
 };
 
 struct ItemIter {
   long long f, fb, fe;
-  int p, i;
+  int p, i, solo;
 };
+
+// The q-th K/V load of an item: key tile j (relative to the item's first)
+// and which = 0 (K) or 1 (V).  Paired items load K_j, V_j for j in order.
+// Solo items (len key tiles, alternating between the two halves) load K_0,
+// then K_{j+1} before V_j: K_0, K_1, V_0, K_2, V_1, ..., K_{len-1}, V_{len-2},
+// V_{len-1}.  A half holds its V until its next group, so the K it needs
+// next must not queue behind it in the ring.
+__device__ __forceinline__ void load_order(bool solo, int len, int q, int& j, int& which) {
+  if (!solo) {
+    j = q >> 1;
+    which = q & 1;
+    return;
+  }
+  if (q == 0) {
+    j = 0;
+    which = 0;
+    return;
+  }
+  const int r = q - 1, m = r >> 1;
+  if (r & 1) {
+    j = m;
+    which = 1;
+  } else if (m + 1 < len) {
+    j = m + 1;
+    which = 0;
+  } else {
+    j = len - 1;
+    which = 1;
+  }
+}
 
 __device__ __forceinline__ int row_limit_dev(const int32_t* offs, int n_blocks, int token) {
   int lo = 0, hi = n_blocks - 1;
@@ -225,7 +269,19 @@ __device__ __forceinline__ int row_limit_dev(const int32_t* offs, int n_blocks, 
 }
 
 __device__ __forceinline__ void iter_init(const Params& P, const Dims& D, ItemIter& it) {
+  it.solo = 0;
   if (!P.prefill) {
+    const int paired = P.solo ? D.groups * P.pairs : static_cast<int>(gridDim.x);
+    if (static_cast<int>(blockIdx.x) >= paired) {
+      // a solo CTA: the unpaired last query tile, over its own group ranges
+      const int g = static_cast<int>(blockIdx.x) - paired;
+      it.solo = 1;
+      it.p = P.pairs;
+      it.fb = static_cast<long long>(g) * D.work / P.solo_groups;
+      it.fe = static_cast<long long>(g + 1) * D.work / P.solo_groups;
+      it.f = it.fb;
+      return;
+    }
     const int g = blockIdx.x / P.pairs;
     it.p = blockIdx.x % P.pairs;
     if (g < D.groups && 2 * it.p * BM < D.q_len) {
@@ -254,8 +310,14 @@ __device__ __forceinline__ bool iter_next(const Params& P, const Dims& D, ItemIt
     item.t0 = t0;
     item.slot = (t0 == 0 && t1 == D.kv_tiles) ? -1
                                               : (h == static_cast<int>(it.fb / D.kv_tiles) ? 0 : 1);
-    for (int t = 0; t < 2; ++t)
-      item.n[t] = ((2 * it.p + t) * BM < D.q_len) ? (t1 - t0) : 0;
+    item.solo = it.solo;
+    if (it.solo) {
+      item.n[0] = (t1 - t0 + 1) / 2;
+      item.n[1] = (t1 - t0) / 2;
+    } else {
+      for (int t = 0; t < 2; ++t)
+        item.n[t] = ((2 * it.p + t) * BM < D.q_len) ? (t1 - t0) : 0;
+    }
     it.f += t1 - t0;
     return true;
   }
@@ -264,6 +326,7 @@ __device__ __forceinline__ bool iter_next(const Params& P, const Dims& D, ItemIt
   item.pair = P.pairs - 1 - it.i % P.pairs;   // longest key range first
   item.t0 = 0;
   item.slot = -1;
+  item.solo = 0;
   for (int t = 0; t < 2; ++t) {
     const int r0 = (2 * item.pair + t) * BM;
     if (r0 < D.q_len) {
@@ -437,6 +500,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(BAR_DRAIN), 1);
     mbar_init(bar(BAR_DRAIN + 1), 1);
     mbar_init(bar(BAR_STALL), 1);
+    mbar_init(bar(BAR_MERGE), 128);
+    mbar_init(bar(BAR_MERGE_FREE), 128);
     *abort_flag = 0;
     *issue_lk = 0;
     *loads_issued = 0;
@@ -477,7 +542,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (!wait_bar(bar(BAR_Q_EMPTY), q_phase ^ 1u, abort_flag, P.timeout_ns, W_PROD_QE)) break;
         q_phase ^= 1u;
         ++q_issued;
-        const int ntiles = (item.n[1] > 0) ? 2 : 1;
+        // a solo item has one query tile, whose key tiles alternate between
+        // the two halves: the ring carries all of them once, in order
+        const int ntiles = (!item.solo && item.n[1] > 0) ? 2 : 1;
         mbar_arrive_expect_tx(bar(BAR_Q_FULL), ntiles * TILE_BYTES);
         for (int t = 0; t < ntiles; ++t) {
           const int row0 = (2 * item.pair + t) * BM;
@@ -485,12 +552,14 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             tma_load_2d(sQ + t * TILE_BYTES + hf * HALF_BYTES, &tm_q, bar(BAR_Q_FULL),
                         item.h * HD + hf * 64, row0);
         }
-        const int n_iter = max(item.n[0], item.n[1]);
-        for (int j = 0; j < n_iter && ok; ++j) {
+        const int n_loads = 2 * (item.solo ? item.n[0] + item.n[1] : max(item.n[0], item.n[1]));
+        for (int q = 0; q < n_loads && ok; ++q) {
+          int j, which;
+          load_order(item.solo, item.n[0] + item.n[1], q, j, which);
           const int tile = item.t0 + j;
           const bool from_side = P.side && tile >= P.kv_tiles_c;
           const int kv0 = (from_side ? tile - P.kv_tiles_c : tile) * BN;
-          for (int which = 0; which < 2; ++which) {
+          {
             if (!wait_bar(bar(BAR_KV_EMPTY + ring.stage), ring.phase ^ 1u, abort_flag,
                           P.timeout_ns, W_PROD_KVE)) {
               ok = false;
@@ -554,15 +623,16 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       uint32_t q_phase = 0, p_phase = 0, of_phase = 0;
       bool ok = true;
 
-      auto issue_qk = [&](uint32_t kslot) {
+      auto issue_qk_from = [&](uint32_t qaddr, uint32_t kslot) {
         const uint32_t b0 = sKV + kslot * TILE_BYTES;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-          mma_ss(tS, smem_desc_sw128(aQ + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024),
+          mma_ss(tS, smem_desc_sw128(qaddr + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024),
                  IDESC_QK, k > 0 ? 1u : 0u);
         }
       };
+      auto issue_qk = [&](uint32_t kslot) { issue_qk_from(aQ, kslot); };
       auto issue_pv = [&](uint32_t vslot, bool acc) {
         const uint32_t b0 = sKV + vslot * TILE_BYTES;
 #pragma unroll
@@ -579,8 +649,81 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         ok = false;
       }
       while (ok && iter_next(P, D, it, item)) {
+        if (item.solo) {
+          // One query tile (in Q slot 0) on both halves; this issuer owns the
+          // key tiles j = t, t + 2, ...  It walks the whole ring in the
+          // producer's order (load_order), waiting for each slot to fill
+          // before releasing it: the other half's slots at once, its own K
+          // after its QK, its own V after its PV.  At each own K: PV of the
+          // previous own tile (once its P is in) and QK of this one, as one
+          // group under the issue lock; the last PV follows the walk.
+          const int len = item.n[0] + item.n[1];
+          if (!wait_bar(bar(BAR_Q_FULL), q_phase, abort_flag, P.timeout_ns, W_MMA_Q)) break;
+          q_phase ^= 1u;
+          uint32_t pend_v = NSTAGE;   // V slot of the last own tile (its PV pending); none yet
+          int pvs = 0;                // PVs issued in this item
+          bool bad = false;
+#pragma unroll 1
+          for (int q = 0; q <= 2 * len; ++q) {
+            // q == 2 * len: past the walk, the last own tile's PV alone
+            const bool last = q == 2 * len;
+            int j = 0, which = 0;
+            uint32_t slot = 0;
+            if (!last) {
+              load_order(true, len, q, j, which);
+              slot = ring.stage;
+              if (!wait_bar(bar(BAR_KV_FULL + slot), ring.phase, abort_flag, P.timeout_ns, W_MMA_KV)) {
+                bad = true;
+                break;
+              }
+              ring.advance();
+              if ((j & 1) != t) {               // the other half's tile
+                mbar_arrive(bar(BAR_KV_EMPTY + slot));
+                continue;
+              }
+              if (which == 1) {                 // own V: held until its PV
+                pend_v = slot;
+                continue;
+              }
+            } else if (pend_v == NSTAGE) {
+              break;                            // no own tile at all
+            }
+            if (pend_v != NSTAGE) {
+              if (!wait_bar(bar(BAR_P_FULL + t), p_phase, abort_flag, P.timeout_ns, W_MMA_P)) {
+                bad = true;
+                break;
+              }
+              p_phase ^= 1u;
+              if (pvs == 0) {   // the item's first PV: the last epilogue must have read O
+                if (!wait_bar(bar(BAR_O_FREE + t), of_phase ^ 1u, abort_flag, P.timeout_ns, W_MMA_OF)) {
+                  bad = true;
+                  break;
+                }
+                of_phase ^= 1u;
+              }
+            }
+            tc_fence_after();
+            if (!issue_lock(issue_lk, abort_flag, P.timeout_ns)) { bad = true; break; }
+            if (pend_v != NSTAGE) issue_pv(pend_v, pvs > 0);
+            if (!last) issue_qk_from(sQ, slot);
+            mma_commit(bar(last ? BAR_O_FULL + t : BAR_S_FULL + t));
+            issue_unlock(issue_lk);
+            if (pend_v != NSTAGE) {
+              mma_commit(bar(BAR_KV_EMPTY + pend_v));
+              pend_v = NSTAGE;
+              ++pvs;
+            }
+            if (!last) {
+              mma_commit(bar(BAR_KV_EMPTY + slot));
+              if (j + 2 >= len) mma_commit(bar(BAR_Q_EMPTY));   // this issuer's last QK
+            }
+          }
+          if (bad) { ok = false; break; }
+          if ((t ? item.n[1] : item.n[0]) == 0) mbar_arrive(bar(BAR_Q_EMPTY));   // no QK of ours on this Q
+          continue;
+        }
         const int n_iter = max(item.n[0], item.n[1]);
-        const int n = item.n[t];
+        const int n = t ? item.n[1] : item.n[0];
         if (!wait_bar(bar(BAR_Q_FULL), q_phase, abort_flag, P.timeout_ns, W_MMA_Q)) break;
         q_phase ^= 1u;
         // prologue: QK_t(0)
@@ -739,15 +882,16 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 256u * t;
     const uint32_t tO = tS + 128u;
-    uint32_t s_phase = 0, o_phase = 0;
+    uint32_t s_phase = 0, o_phase = 0, merge_phase = 0;
     ItemIter it;
     iter_init(P, D, it);
     Item item;
     bool ok = true;
     while (ok && iter_next(P, D, it, item)) {
-      const int n = item.n[t];
-      if (n == 0) continue;
-      const int row = (2 * item.pair + t) * BM + r_in_tile;   // local query row
+      const int n = t ? item.n[1] : item.n[0];
+      if (n == 0 && !item.solo) continue;
+      // local query row (a solo item's two halves share the one tile's rows)
+      const int row = (2 * item.pair + (item.solo ? 0 : t)) * BM + r_in_tile;
       const bool valid = row < D.q_len;
       const int e_row = (P.prefill && valid) ? row_limit_dev(P.offs, P.n_blocks, P.q_row0 + row)
                                              : D.kv_len;
@@ -765,7 +909,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 4; ++c) tmem_reg_fence(s[c]);
 
         // key range of this tile and the limit its columns are masked at
-        const int tile = item.t0 + jj;
+        // (a solo item's half t takes every other key tile, from t on)
+        const int tile = item.t0 + (item.solo ? 2 * jj + t : jj);
         int kv0 = tile * BN, e_lim = e_row;
         if (P.side) {
           if (tile < P.kv_tiles_c) {
@@ -854,12 +999,47 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       if (!ok) break;
       // ---- epilogue: O_t / l
-      const bool got = wait_bar(bar(BAR_O_FULL + t), o_phase, abort_flag, P.timeout_ns, W_SM_O);
-      if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
-      o_phase ^= 1u;
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      const float lse2 = m + __log2f(l);
+      if (n > 0) {
+        const bool got = wait_bar(bar(BAR_O_FULL + t), o_phase, abort_flag, P.timeout_ns, W_SM_O);
+        if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+        o_phase ^= 1u;
+      }
+      // A solo item's half 1 hands its row (m, l) to half 0 through shared
+      // memory and is done; half 0 merges both halves' O (same rows, same
+      // TMEM lanes) and frees both accumulators:
+      //   M = max(m0, m1), a_i = 2^(m_i - M), O = (a0 O0 + a1 O1) / (a0 l0 + a1 l1).
+      float* merge_ml = reinterpret_cast<float*>(sgen + SMEM_MERGE);
+      if (item.solo && t == 1) {
+        // the previous solo item's values must have been read by half 0
+        const bool freed = wait_bar(bar(BAR_MERGE_FREE), merge_phase ^ 1u, abort_flag, P.timeout_ns,
+                                    W_SM_MERGE);
+        if (__any_sync(0xffffffffu, !freed)) { ok = false; break; }
+        merge_ml[r_in_tile] = n > 0 ? m : -INFINITY;
+        merge_ml[BM + r_in_tile] = n > 0 ? l : 0.f;
+        tc_fence_before();
+        mbar_arrive(bar(BAR_MERGE));
+        merge_phase ^= 1u;
+        continue;
+      }
+      float f0 = 1.f / l, f1 = 0.f, lse2 = m + __log2f(l);
+      bool two = false;
+      if (item.solo) {
+        const bool got = wait_bar(bar(BAR_MERGE), merge_phase, abort_flag, P.timeout_ns, W_SM_MERGE);
+        if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
+        merge_phase ^= 1u;
+        tc_fence_after();
+        const float m1 = merge_ml[r_in_tile], l1 = merge_ml[BM + r_in_tile];
+        mbar_arrive(bar(BAR_MERGE_FREE));
+        two = item.n[1] > 0;
+        const float mx = fmaxf(m, m1);
+        const float a0 = ex2_approx(m - mx);
+        const float a1 = l1 > 0.f ? ex2_approx(m1 - mx) : 0.f;
+        const float lt = l * a0 + l1 * a1;
+        f0 = a0 / lt;
+        f1 = a1 / lt;
+        lse2 = mx + __log2f(lt);
+      }
+      const uint32_t tO1 = tO + 256u;   // half 1's accumulator (solo items)
       if (item.slot < 0) {
         __nv_bfloat16* dst = P.out + (static_cast<size_t>(row) * P.heads + item.h) * HD;
         const bool put = valid && WS_BOUND(g_attn_error, (static_cast<long long>(row) * P.heads + item.h) * HD,
@@ -869,15 +1049,26 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           uint32_t o[32];
           tmem_ld32(tO + 32u * c, o);
           tmem_ld_wait(o);
+          if (two) {
+            uint32_t o1[32];
+            tmem_ld32(tO1 + 32u * c, o1);
+            tmem_ld_wait(o1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(fmaf(__uint_as_float(o1[i]), f1, __uint_as_float(o[i]) * f0));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f0);
+          }
           if (put) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+              w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]), __uint_as_float(o[8 * q + 1]));
+              w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]), __uint_as_float(o[8 * q + 3]));
+              w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]), __uint_as_float(o[8 * q + 5]));
+              w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]), __uint_as_float(o[8 * q + 7]));
               d4[q] = w;
             }
           }
@@ -888,7 +1079,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           P.lse[static_cast<size_t>(item.h) * D.lse_stride + row] = lse2 * LN2;
       } else {
         const size_t slot = static_cast<size_t>(blockIdx.x) * 2 + item.slot;
-        const size_t prow = slot * 256 + t * BM + r_in_tile;
+        const size_t prow = slot * 256 + (item.solo ? 0 : t) * BM + r_in_tile;
         float* dst = P.ws_o + prow * HD;
         const bool put = valid && WS_BOUND(g_attn_error, prow, static_cast<long long>(gridDim.x) * 512, 23);
 #pragma unroll 1
@@ -896,26 +1087,41 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           uint32_t o[32];
           tmem_ld32(tO + 32u * c, o);
           tmem_ld_wait(o);
+          if (two) {
+            uint32_t o1[32];
+            tmem_ld32(tO1 + 32u * c, o1);
+            tmem_ld_wait(o1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(fmaf(__uint_as_float(o1[i]), f1, __uint_as_float(o[i]) * f0));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f0);
+          }
           if (put) {
             float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              d4[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                                  __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+              d4[q] = make_float4(__uint_as_float(o[4 * q + 0]), __uint_as_float(o[4 * q + 1]),
+                                  __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
           }
         }
         if (put) P.ws_lse[prow] = lse2;
       }
       tc_fence_before();
       mbar_arrive(bar(BAR_O_FREE + t));
+      if (two) mbar_arrive(bar(BAR_O_FREE + 1));   // half 1's accumulator, read above
     }
   }
 
+  // Teardown.  The TMEM address and the warp index are read afresh, so no
+  // value stays live through the role branches (one that did would need the
+  // same register under both register budgets, and spill in one of them).
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if ((threadIdx.x >> 5) == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), TMEM_COLS);
   }
 }
 
@@ -949,16 +1155,22 @@ attn_combine_kernel(Params P) {
   if (!load_dims(P, D)) return;
   const int h = blockIdx.y;
   const long long L = D.kv_tiles;
-  const int g_lo = group_of(h * L, D.work, D.groups);
-  const int g_hi = group_of((h + 1) * L - 1, D.work, D.groups);
+  // Rows of the unpaired last query tile (solo CTAs) have their own groups,
+  // after the paired CTAs; a block of 32 rows lies wholly on one side.
+  const int solo_row0 = 2 * BM * P.pairs;
+  const bool solo_rows = P.solo && static_cast<int>(blockIdx.x) * COMBINE_ROWS >= solo_row0;
+  const int groups = solo_rows ? P.solo_groups : D.groups;
+  const int g_lo = group_of(h * L, D.work, groups);
+  const int g_hi = group_of((h + 1) * L - 1, D.work, groups);
   if (g_lo == g_hi) return;   // one group covered the head: final output already written
   const int cnt = g_hi - g_lo + 1;
-  // slot index (partial row block) of group g: (g * pairs + pair) * 2 + slot,
-  // stored without the pair term, which depends on the row
+  // slot index (partial row block) of group g: paired rows (g * pairs + pair)
+  // * 2 + slot, stored without the pair term, which depends on the row; solo
+  // rows (groups * pairs + g) * 2 + slot
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
     const int g = g_lo + i;
-    const int slot = (h == static_cast<int>(group_begin(g, D.work, D.groups) / L)) ? 0 : 1;
-    s_gs[i] = g * 2 * P.pairs + slot;
+    const int slot = (h == static_cast<int>(group_begin(g, D.work, groups) / L)) ? 0 : 1;
+    s_gs[i] = solo_rows ? (D.groups * P.pairs + g) * 2 + slot : g * 2 * P.pairs + slot;
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5;
@@ -988,8 +1200,13 @@ attn_combine_kernel(Params P) {
         l[k][u] = -INFINITY;
         o[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row < D.q_len && i0 + u < cnt) {
-          const size_t prow = static_cast<size_t>(s_gs[i0 + u] + 2 * (row >> 8)) * 256 + (row & 255);
-          if (!WS_BOUND(g_attn_error, prow, static_cast<long long>(P.groups) * P.pairs * 512, 24)) continue;
+          const size_t prow = solo_rows
+              ? static_cast<size_t>(s_gs[i0 + u]) * 256 + (row - solo_row0)
+              : static_cast<size_t>(s_gs[i0 + u] + 2 * (row >> 8)) * 256 + (row & 255);
+          if (!WS_BOUND(g_attn_error, prow,
+                        (static_cast<long long>(P.groups) * P.pairs + (P.solo ? P.solo_groups : 0)) * 512,
+                        24))
+            continue;
           l[k][u] = ws_lse[prow];
           o[k][u] = reinterpret_cast<const float4*>(ws_o + prow * HD)[lane];
         }
@@ -1039,8 +1256,35 @@ long long host_group_of(long long f, long long work, int groups) {
 
 }  // namespace
 
+namespace {
+
+// Groups of CTAs over `work` (head, key tile) units: at most `cap`; with at
+// least one group per head, a multiple of the head count, so that every
+// head's key range splits evenly on head boundaries, one work item per CTA
+// (the 192x336 unit: 72 groups of a third of a head, 9.5% faster than 74
+// groups whose ranges straddle heads).
+long long plan_groups(long long cap, int heads, long long work) {
+  long long g = cap;
+  if (g >= heads) g = (g / heads) * heads;
+  if (g < 1) g = 1;
+  if (g > work) g = work;
+  if (g > COMBINE_MAX_GROUPS) g = COMBINE_MAX_GROUPS;   // the merge lists a head's groups in smem
+  return g;
+}
+
+bool any_head_split(long long kv_tiles, int heads, long long work, long long groups) {
+  for (int h = 0; h < heads; ++h) {
+    const long long lo = host_group_of(static_cast<long long>(h) * kv_tiles, work, groups);
+    const long long hi = host_group_of(static_cast<long long>(h + 1) * kv_tiles - 1, work, groups);
+    if (lo != hi) return true;
+  }
+  return false;
+}
+
+}  // namespace
+
 bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0, int kv_len,
-                  int n_blocks, int num_sms, int side_len) {
+                  int n_blocks, int num_sms, int side_len, bool allow_solo) {
   p = TcAttnPlan{};
   p.prefill = prefill ? 1 : 0;
   p.heads = heads;
@@ -1069,24 +1313,28 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
     return true;
   }
   p.work = static_cast<long long>(heads) * p.kv_tiles;
-  long long g = num_sms / p.pairs;
-  // With at least one group per head, use a multiple of the head count: every
-  // head's key range then splits evenly on head boundaries, one work item per
-  // CTA (the 192x336 unit: 72 groups of a third of a head, 9.5% faster than
-  // 74 groups whose ranges straddle heads).
-  if (g >= heads) g = (g / heads) * heads;
-  if (g < 1) g = 1;
-  if (g > p.work) g = p.work;
-  if (g > COMBINE_MAX_GROUPS) g = COMBINE_MAX_GROUPS;   // the merge lists a head's groups in smem
-  p.groups = static_cast<int>(g);
-  const long long grid = g * p.pairs;
-  if (grid > (1LL << 30)) return false;
-  p.grid = static_cast<int>(grid);
-  p.split = false;
-  for (int h = 0; h < heads && !p.split; ++h) {
-    const long long lo = host_group_of(static_cast<long long>(h) * p.kv_tiles, p.work, p.groups);
-    const long long hi = host_group_of(static_cast<long long>(h + 1) * p.kv_tiles - 1, p.work, p.groups);
-    p.split = lo != hi;
+  if (allow_solo && (p.qtiles & 1)) {
+    // The last query tile is unpaired: it gets solo CTAs, which run a key
+    // range at twice the rate of a paired CTA, so they get half as many
+    // groups of twice the range: full pairs * 2G + G CTAs in all.
+    p.solo = 1;
+    p.pairs = p.qtiles / 2;
+    const long long g1 = plan_groups(num_sms / (2 * p.pairs + 1), heads, p.work);
+    const long long g0 = p.pairs > 0 ? plan_groups(2 * g1, heads, p.work) : 0;
+    p.groups = static_cast<int>(g0);
+    p.solo_groups = static_cast<int>(g1);
+    const long long grid = g0 * p.pairs + g1;
+    if (grid > (1LL << 30) || grid > num_sms) return false;
+    p.grid = static_cast<int>(grid);
+    p.split = any_head_split(p.kv_tiles, heads, p.work, g1) ||
+              (g0 > 0 && any_head_split(p.kv_tiles, heads, p.work, g0));
+  } else {
+    const long long g = plan_groups(num_sms / p.pairs, heads, p.work);
+    p.groups = static_cast<int>(g);
+    const long long grid = g * p.pairs;
+    if (grid > (1LL << 30)) return false;
+    p.grid = static_cast<int>(grid);
+    p.split = any_head_split(p.kv_tiles, heads, p.work, g);
   }
   p.workspace_bytes = p.split ? static_cast<size_t>(p.grid) * 2 * 256 * (HD + 1) * sizeof(float) : 0;
   return true;
@@ -1160,6 +1408,8 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   // q_max) and the whole cache (kv_len = capacity)
   P.dev_state = a.dev_state;
   P.q_max = plan.q_len;
+  P.solo = plan.solo;
+  P.solo_groups = plan.solo_groups;
   attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs, P);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

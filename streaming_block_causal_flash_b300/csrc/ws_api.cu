@@ -271,7 +271,7 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
 size_t dev_workspace_bytes(int64_t q_max, int64_t capacity, int num_heads, int sms) {
   ws::TcAttnPlan plan;
   if (!ws::plan_tc_attn(plan, false, num_heads, (int)q_max, (int)(capacity - q_max), (int)capacity,
-                        1, sms))
+                        1, sms, 0, false))
     return 0;
   ws::plan_force_split(plan);
   return plan.workspace_bytes;
@@ -505,7 +505,7 @@ ws_status ws_block_causal_attn_dev(const void* q, const void* k_cache, const voi
   if (sms <= 0) return fail(WS_ERR_CUDA, "%s: cannot query the current device", who);
   ws::TcAttnPlan plan;
   if (!ws::plan_tc_attn(plan, false, num_heads, (int)q_max, (int)(capacity - q_max), (int)capacity,
-                        1, sms))
+                        1, sms, 0, false))
     return fail(WS_ERR_INVALID_ARGUMENT, "%s: sizes out of range", who);
   ws::plan_force_split(plan);
   if (workspace_bytes < plan.workspace_bytes)

@@ -87,10 +87,15 @@ struct TcAttnPlan {
   size_t workspace_bytes;
   int side_len;      // unit mode: keys of the newest block read from side buffers (0: none)
   int kv_tiles_c;    // side mode: key tiles of the cache part
+  int solo;          // unit mode, odd tile count: the last query tile has solo CTAs
+                     // (pairs then counts the full pairs, groups the paired groups)
+  int solo_groups;   // groups of solo CTAs
 };
 // Fills the plan for the given sizes; returns false when the sizes do not fit.
+// allow_solo: give an unpaired last query tile CTAs of its own (host-sized
+// unit launches; launches sized for the largest unit keep plain pairs).
 bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0, int kv_len,
-                  int n_blocks, int num_sms, int side_len = 0);
+                  int n_blocks, int num_sms, int side_len = 0, bool allow_solo = true);
 
 struct TcAttnArgs {
   const void* q;
