@@ -1081,7 +1081,9 @@ def measure_unit_brief(name: str, device, peaks, steps: int = 10, warmup: int = 
 def measure_other_workloads(device, peaks, exclude: str):
     """Brief measurements of every bf16 workload but the line's own."""
     res = {}
-    for name, w in WORKLOADS.items():
+    # streaming units first, the prefill (which heats the GPU most) last
+    order = sorted(WORKLOADS.items(), key=lambda kv: kv[1].prefill)
+    for name, w in order:
         if w.dtype != "bf16" or name == exclude:
             continue
         if w.prefill:
