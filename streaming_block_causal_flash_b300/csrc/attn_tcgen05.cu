@@ -13,7 +13,8 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q tiles once per work item, then K_j, V_j into a
 //              5-slot ring of 32 KB slots (128 rows x 128 cols, two 128-byte
-//              swizzled column halves)
+//              swizzled column halves); 6 slots in solo CTAs (below), which
+//              need one Q slot only
 //   warp  9    TMEM owner; its lane 0 issues every MMA of query tile 0
 //   warp  10   lane 0 issues every MMA of query tile 1 (two issuers keep the
 //              tensor pipe fed while the other one waits on barriers)
@@ -51,6 +52,11 @@
 //    nearly the same time (one HBM read, L2 reuse).  A range that covers only
 //    part of a head writes a partial (O/l, log2-sum-exp) into the workspace;
 //    attn_combine_kernel merges the partials.
+//    With an odd number of query tiles (host-sized launches), the last tile
+//    gets solo CTAs of its own: both TMEM halves work on that one tile, on
+//    alternate key tiles of the range, and the epilogue merges the two
+//    halves' (m, l, O).  A solo CTA runs a range at about twice a paired
+//    CTA's rate, so it gets twice the range (half as many groups).
 //    Side mode (unit mode only): keys [0, cache_len) come from the cache and
 //    the newest unit's keys from token-major side buffers through 2-D TMA
 //    maps; the two parts are tiled separately, each with its own ragged tail.
@@ -82,7 +88,10 @@ namespace {
 constexpr int BM = 128;                       // query rows per tile
 constexpr int BN = 128;                       // keys per tile
 constexpr int HD = 128;                       // head dim
-constexpr int NSTAGE = 5;                     // K/V ring slots
+constexpr int NSTAGE = 5;                     // K/V ring slots (paired CTAs)
+// Solo CTAs hold one query tile; the second Q slot, which follows the ring in
+// shared memory, becomes a sixth ring slot for them.
+constexpr int NSTAGE_SOLO = NSTAGE + 1;
 constexpr int TILE_BYTES = BM * HD * 2;       // 32 KB
 constexpr int HALF_BYTES = TILE_BYTES / 2;    // 128 rows x 64 cols (128-byte rows)
 constexpr int NUM_THREADS = 384;
@@ -104,8 +113,8 @@ constexpr unsigned long long DRAIN_TIMEOUT_NS = 2000000000ull;
 
 // barrier indices
 constexpr int BAR_KV_FULL = 0;
-constexpr int BAR_KV_EMPTY = NSTAGE;
-constexpr int BAR_Q_FULL = 2 * NSTAGE;
+constexpr int BAR_KV_EMPTY = NSTAGE_SOLO;
+constexpr int BAR_Q_FULL = 2 * NSTAGE_SOLO;
 constexpr int BAR_Q_EMPTY = BAR_Q_FULL + 1;
 constexpr int BAR_S_FULL = BAR_Q_EMPTY + 1;   // [2]
 constexpr int BAR_P_FULL = BAR_S_FULL + 2;    // [2]
@@ -117,9 +126,11 @@ constexpr int BAR_MERGE = BAR_STALL + 1;      // solo items: half 1's (m, l) are
 constexpr int BAR_MERGE_FREE = BAR_MERGE + 1; // solo items: half 0 has read them
 constexpr int NUM_BARS = BAR_MERGE_FREE + 1;
 
+// Q slot 0, the K/V ring, Q slot 1 (ring slot NSTAGE of solo CTAs)
 constexpr int SMEM_Q = 0;
-constexpr int SMEM_KV = 2 * TILE_BYTES;
-constexpr int SMEM_BARS = SMEM_KV + NSTAGE * TILE_BYTES;
+constexpr int SMEM_KV = TILE_BYTES;
+constexpr int SMEM_Q1 = SMEM_KV + NSTAGE * TILE_BYTES;
+constexpr int SMEM_BARS = SMEM_Q1 + TILE_BYTES;
 constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;
 // tmem slot, abort flag, issue lock, loads issued; then the launch's sizes;
 // then a solo item's per-row (m, l) of TMEM half 1
@@ -444,10 +455,14 @@ __device__ __forceinline__ void exp_pass(uint32_t (&s)[4][32], uint64_t sc2, flo
   }
 }
 
+// A slot index that names no ring slot.
+constexpr uint32_t NO_SLOT = 0xFFu;
+
 struct Ring {
-  uint32_t stage = 0, phase = 0;
+  uint32_t stage, phase, n;   // n: slots in the ring (NSTAGE or NSTAGE_SOLO)
+  __device__ __forceinline__ explicit Ring(uint32_t slots) : stage(0), phase(0), n(slots) {}
   __device__ __forceinline__ void advance() {
-    if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+    if (++stage == n) { stage = 0; phase ^= 1u; }
   }
 };
 
@@ -468,6 +483,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw);
   const uint32_t sQ = sbase + SMEM_Q;
+  const uint32_t sQ1 = sbase + SMEM_Q1;
   const uint32_t sKV = sbase + SMEM_KV;
   const uint32_t sBar = sbase + SMEM_BARS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + SMEM_MISC);
@@ -484,7 +500,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < NSTAGE_SOLO; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), 1);
       // released by both MMA issuers
       mbar_init(bar(BAR_KV_EMPTY + s), 2);
@@ -534,7 +550,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       ItemIter it;
       iter_init(P, D, it);
       Item item;
-      Ring ring;
+      Ring ring(it.solo ? NSTAGE_SOLO : NSTAGE);
       uint32_t q_phase = 0;
       int issued = 0, q_issued = 0;
       bool ok = true;
@@ -549,7 +565,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int t = 0; t < ntiles; ++t) {
           const int row0 = (2 * item.pair + t) * BM;
           for (int hf = 0; hf < 2; ++hf)
-            tma_load_2d(sQ + t * TILE_BYTES + hf * HALF_BYTES, &tm_q, bar(BAR_Q_FULL),
+            tma_load_2d((t ? sQ1 : sQ) + hf * HALF_BYTES, &tm_q, bar(BAR_Q_FULL),
                         item.h * HD + hf * 64, row0);
         }
         const int n_loads = 2 * (item.solo ? item.n[0] + item.n[1] : max(item.n[0], item.n[1]));
@@ -586,14 +602,14 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
       // Teardown: every copy this warp started must have landed before the
-      // CTA may exit.  The ring slots filled last (up to NSTAGE of them) and
+      // CTA may exit.  The ring slots filled last (up to a ring's worth) and
       // the last Q load are waited for with bounded waits; loads already
       // consumed return at once.
       volatile int no_abort = 0;
-      const int pend = issued < NSTAGE ? issued : NSTAGE;
+      const int pend = issued < static_cast<int>(ring.n) ? issued : static_cast<int>(ring.n);
       Ring back = ring;
       for (int k = 0; k < pend; ++k) {
-        if (back.stage == 0) { back.stage = NSTAGE - 1; back.phase ^= 1u; }
+        if (back.stage == 0) { back.stage = back.n - 1; back.phase ^= 1u; }
         else --back.stage;
         wait_bar(bar(BAR_KV_FULL + back.stage), back.phase, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_TMA);
       }
@@ -613,13 +629,13 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int t = warp - 9;
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, 0, 1);
-      const uint32_t aQ = sQ + t * TILE_BYTES;
+      const uint32_t aQ = t ? sQ1 : sQ;
       const uint32_t tS = tmem + 256u * t;
       const uint32_t tO = tS + 128u;
       ItemIter it;
       iter_init(P, D, it);
       Item item;
-      Ring ring;
+      Ring ring(it.solo ? NSTAGE_SOLO : NSTAGE);
       uint32_t q_phase = 0, p_phase = 0, of_phase = 0;
       bool ok = true;
 
@@ -660,7 +676,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           const int len = item.n[0] + item.n[1];
           if (!wait_bar(bar(BAR_Q_FULL), q_phase, abort_flag, P.timeout_ns, W_MMA_Q)) break;
           q_phase ^= 1u;
-          uint32_t pend_v = NSTAGE;   // V slot of the last own tile (its PV pending); none yet
+          uint32_t pend_v = NO_SLOT;  // V slot of the last own tile (its PV pending); none yet
           int pvs = 0;                // PVs issued in this item
           bool bad = false;
 #pragma unroll 1
@@ -685,10 +701,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                 pend_v = slot;
                 continue;
               }
-            } else if (pend_v == NSTAGE) {
+            } else if (pend_v == NO_SLOT) {
               break;                            // no own tile at all
             }
-            if (pend_v != NSTAGE) {
+            if (pend_v != NO_SLOT) {
               if (!wait_bar(bar(BAR_P_FULL + t), p_phase, abort_flag, P.timeout_ns, W_MMA_P)) {
                 bad = true;
                 break;
@@ -704,13 +720,13 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             tc_fence_after();
             if (!issue_lock(issue_lk, abort_flag, P.timeout_ns)) { bad = true; break; }
-            if (pend_v != NSTAGE) issue_pv(pend_v, pvs > 0);
+            if (pend_v != NO_SLOT) issue_pv(pend_v, pvs > 0);
             if (!last) issue_qk_from(sQ, slot);
             mma_commit(bar(last ? BAR_O_FULL + t : BAR_S_FULL + t));
             issue_unlock(issue_lk);
-            if (pend_v != NSTAGE) {
+            if (pend_v != NO_SLOT) {
               mma_commit(bar(BAR_KV_EMPTY + pend_v));
-              pend_v = NSTAGE;
+              pend_v = NO_SLOT;
               ++pvs;
             }
             if (!last) {
