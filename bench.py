@@ -38,8 +38,12 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "unit_640x368"
 L2_BYTES = 126 * 1024 * 1024
 ATTN_SOURCE = os.path.join(ROOT, "streaming_block_causal_flash_b300", "csrc", "attn_tcgen05.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_tcgen05_unit_640x368_traffic.txt")
-TRAFFIC_WORKLOAD = "unit_640x368"
+PROFILES_DIR = os.path.join(ROOT, "profiles")
+
+
+def traffic_file(workload: str) -> str:
+    """The committed ncu summary of one attention launch's DRAM bytes for a workload."""
+    return os.path.join(PROFILES_DIR, f"attn_tcgen05_{workload}_traffic.txt")
 
 
 # ----------------------------------------------------------------- plumbing
@@ -312,13 +316,14 @@ def source_digest(path: str) -> str:
 
 
 def recorded_traffic(workload: str = DEFAULT_WORKLOAD):
-    """DRAM bytes per attention launch from the committed ncu summary, or None
-    when the kernel source changed since those counters were taken or the
-    summary covers another workload."""
-    if workload != TRAFFIC_WORKLOAD or not os.path.exists(TRAFFIC_FILE):
+    """DRAM bytes per attention launch from the workload's committed ncu
+    summary, or None when there is none or the kernel source changed since
+    its counters were taken."""
+    path = traffic_file(workload)
+    if not os.path.exists(path):
         return None
     vals = {}
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line:
                 k, v = line.split(":", 1)
@@ -1015,7 +1020,8 @@ def prefill_measure(K: int, W: int, w: Workload, device, rank, world, peaks, wit
                        "l2": f"inputs larger than L2 (K/V {2 * H * T * D * 2 / 1e9:.2f} GB)"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "traffic": recorded_traffic(w.name),
                          "kernel": "attn_tc_bf16_kernel, prefill mode (one ws_block_causal_prefill call)",
                          "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4)},
             "gpu_launches": 2 * K, "clocks": clk,

@@ -50,9 +50,9 @@ def test_default_arguments_are_the_unit_640x368_bench():
 
 
 def test_recorded_traffic_is_null_when_kernel_changed(tmp_path, monkeypatch):
-    f = tmp_path / "t.txt"
+    monkeypatch.setattr(bench, "PROFILES_DIR", str(tmp_path))
+    f = tmp_path / "attn_tcgen05_unit_640x368_traffic.txt"
     f.write_text("dram_bytes_per_launch: 123\nkernel_source_sha256_16: deadbeef\n")
-    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
     assert bench.recorded_traffic() is None
     f.write_text(f"dram_bytes_per_launch: 123\nkernel_source_sha256_16: {bench.source_digest(bench.ATTN_SOURCE)}\n")
     assert bench.recorded_traffic() == 123.0
