@@ -667,13 +667,15 @@ def time_attn_side(sess: UnitSession, device, peaks, reps: int = 20):
                       f"timed the same way"}
 
 
-def time_fused_unit(sess: UnitSession, device, reps: int = 50, rounds: int = 3):
+def time_fused_unit(sess: UnitSession, device, reps: int = 20, rounds: int = 4,
+                    rest_s: float = 0.5):
     """The unit step with the append fused into the attention (one
     ws_block_causal_attn_side call that reads the unit's K/V from its slice
-    and, in the background, commits them to the cache; then the Euler steps)
+    and commits them to the cache from shared memory; then the Euler steps)
     against the plain step (append, attention, Euler steps).  Both
-    graph-replayed, measured in alternation so that they see the same clocks;
-    the best round of each."""
+    graph-replayed in alternation, the order swapped every round and the GPU
+    left idle before each replay, so that neither always runs on the hotter
+    GPU; the best round of each."""
     from streaming_block_causal_flash_b300 import ws
     u = sess.units[0]
     n = sess.sizes[u]
@@ -690,14 +692,16 @@ def time_fused_unit(sess: UnitSession, device, reps: int = 50, rounds: int = 3):
         run_unit(sess, u, st)
 
     best = {"plain": float("inf"), "fused": float("inf")}
-    for _ in range(rounds):
-        best["plain"] = min(best["plain"], graph_time_us(plain, reps, device))
-        best["fused"] = min(best["fused"], graph_time_us(fused, reps, device))
+    for r in range(rounds):
+        for name in (("plain", "fused") if r % 2 == 0 else ("fused", "plain")):
+            time.sleep(rest_s)
+            best[name] = min(best[name], graph_time_us(plain if name == "plain" else fused, reps,
+                                                       device))
     flops = sess.unit_flops(u)
     return {"fused_us_per_unit": round(best["fused"], 1), "plain_us_per_unit": round(best["plain"], 1),
             "fused_value": round(flops / (best["fused"] * 1e-6) / 1e12, 3), "unit": UNIT,
-            "method": f"{reps} unit steps per CUDA graph, fused and plain replayed in alternation, "
-                      f"best of {rounds}"}
+            "method": f"{reps} unit steps per CUDA graph, fused and plain replayed in alternation "
+                      f"(order swapped each round, {rest_s} s idle before each), best of {rounds}"}
 
 
 def time_unit_graph(sess: UnitSession, device, reps: int = 50):

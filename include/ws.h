@@ -138,10 +138,12 @@ WS_API ws_status ws_block_causal_attn(const void* q, const void* k_cache, const 
  *                 writes the side K/V into cache rows [offsets[n_blocks-1],
  *                 offsets[n_blocks]) of every head -- the same bytes
  *                 ws_kv_append would write (the append fused into the
- *                 attention: one warp of every CTA copies an equal share of
- *                 the slices while the attention runs); the solver's last
- *                 step commits the clean slice this way.  Requires
- *                 offsets[n_blocks] <= capacity.
+ *                 attention: each side tile the kernel loads into shared
+ *                 memory for the attention is also stored to the cache by
+ *                 TMA, once per tile, before its slot is reused); the
+ *                 solver's last step commits the clean slice this way.
+ *                 Requires offsets[n_blocks] <= capacity.  Cache rows from
+ *                 offsets[n_blocks] on are not written.
  * The cache must hold blocks 0..n_blocks-2 (offsets[n_blocks-1] <= capacity,
  * else WS_ERR_CAPACITY); rows from offsets[n_blocks-1] on are not read.
  * Other arguments, the workspace (same size query) and errors as
@@ -374,8 +376,9 @@ WS_API const char* ws_last_error(void);
  * waiting for Q, 4 MMA issuer waiting for a K/V tile, 5 MMA issuer waiting
  * for P, 6 for the O accumulator to be free, 7 softmax waiting for S, 8 for
  * the final O, 9 teardown waiting for MMAs, 10 for copies, 11 the test
- * hook's stalled wait, 12 the MMA issue lock, 13 the commit copy of
- * ws_block_causal_attn_side waiting for the producer's progress.  The
+ * hook's stalled wait, 12 the MMA issue lock, 13 (no longer used), 14 a
+ * solo CTA's softmax merging its two halves (an odd number of query tiles),
+ * 15 the KV append waiting for its copy of a token's slice.  The
  * outputs of a launch that gave up are undefined; the context
  * stays usable.  The word stays set until ws_clear_device_error().
  */

@@ -18,10 +18,8 @@
 //   warp  9    TMEM owner; its lane 0 issues every MMA of query tile 0
 //   warp  10   lane 0 issues every MMA of query tile 1 (two issuers keep the
 //              tensor pipe fed while the other one waits on barriers)
-//   warp  11   side mode with commit: copies this CTA's share of the newest
-//              unit's K/V slices into the cache, global to global, in the
-//              background (otherwise idle; it completes the third warpgroup,
-//              which gives up registers to the softmax warpgroups)
+//   warp  11   idle (it completes the third warpgroup, which gives up
+//              registers to the softmax warpgroups)
 // TMEM (512 columns): tile t uses S_t = cols [256t, 256t+128) (fp32 logits,
 // overwritten in place by bf16 P in its first 64 columns) and
 // O_t = cols [256t+128, 256t+256) (fp32 output accumulator).
@@ -60,8 +58,9 @@
 //    Side mode (unit mode only): keys [0, cache_len) come from the cache and
 //    the newest unit's keys from token-major side buffers through 2-D TMA
 //    maps; the two parts are tiled separately, each with its own ragged tail.
-//    With commit, warp 11 of every CTA also copies an equal share of the
-//    side slices into the cache, outside the K/V ring.
+//    With commit, the side tiles are also written to the cache by TMA
+//    stores from their ring slots (one CTA per group stores), before each
+//    slot is released.
 //  * prefill mode: one work item per (head, query-tile pair), head-major,
 //    longest key range first; key tiles no row of a query tile can see are
 //    skipped; CTAs take items round-robin.
@@ -100,7 +99,7 @@ constexpr int NUM_THREADS = 384;
 // the block is launched with (NUM_THREADS x the kernel's register count); the
 // host checks that before every launch.
 constexpr int REGS_SOFTMAX = 208;
-constexpr int REGS_OTHER = 80;
+constexpr int REGS_OTHER = 88;
 constexpr int REGS_NEEDED = 256 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -132,15 +131,18 @@ constexpr int SMEM_KV = TILE_BYTES;
 constexpr int SMEM_Q1 = SMEM_KV + NSTAGE * TILE_BYTES;
 constexpr int SMEM_BARS = SMEM_Q1 + TILE_BYTES;
 constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;
-// tmem slot, abort flag, issue lock, loads issued; then the launch's sizes;
+// tmem slot, abort flag, issue lock, (unused); then the launch's sizes;
 // then a solo item's per-row (m, l) of TMEM half 1
 constexpr int SMEM_MERGE = SMEM_MISC + 16 + 32;
-constexpr int SMEM_USED = SMEM_MERGE + 2 * BM * 4;
+// side mode with commit: per ring slot, the cache row and (head, K or V) of a
+// side tile the producer still has to store from it
+constexpr int SMEM_STORE = SMEM_MERGE + 2 * BM * 4;
+constexpr int SMEM_USED = SMEM_STORE + NSTAGE_SOLO * 8;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 // wait sites (error info)
 enum : int { W_PROD_QE = 1, W_PROD_KVE, W_MMA_Q, W_MMA_KV, W_MMA_P, W_MMA_OF, W_SM_S, W_SM_O,
-             W_DRAIN_MMA, W_DRAIN_TMA, W_FORCED, W_LOCK, W_COMMIT, W_SM_MERGE };
+             W_DRAIN_MMA, W_DRAIN_TMA, W_FORCED, W_LOCK, W_UNUSED_13, W_SM_MERGE };
 
 struct Params {
   int prefill;
@@ -150,14 +152,10 @@ struct Params {
   // kv_tiles_c tiles; the newest block's n_side keys come from the
   // token-major side buffers, in the remaining kv_tiles - kv_tiles_c tiles.
   int side, kv_tiles_c, cache_len, n_side;
-  // Side mode with commit: the store warp copies the side tiles it owns into
-  // cache rows cache_len + (row in the side buffer) of k_cache / v_cache
-  // ([H][capacity][HD]).
+  // Side mode with commit: the side tiles, once in the ring, are also
+  // written to cache rows cache_len + (row in the side buffer) by TMA stores
+  // (maps tm_kc / tm_vc, whose rows end at cache_len + n_side).
   int commit;
-  __nv_bfloat16* k_cache;
-  __nv_bfloat16* v_cache;
-  const void* k_side;   // [n_side][heads][HD], the commit's source
-  const void* v_side;
   long long capacity;
   long long work;
   int n_items;
@@ -473,7 +471,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_ks,
-                    const __grid_constant__ CUtensorMap tm_vs, const Params P) {
+                    const __grid_constant__ CUtensorMap tm_vs,
+                    const __grid_constant__ CUtensorMap tm_kc,
+                    const __grid_constant__ CUtensorMap tm_vc, const Params P) {
   // Sizes of this launch; with device-resident sizes every thread reads the
   // same state, so a launch with nothing to do returns in every thread.
   Dims dims;
@@ -489,8 +489,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + SMEM_MISC + 4);
   int* issue_lk = reinterpret_cast<int*>(sgen + SMEM_MISC + 8);
-  // K/V tile loads the producer has issued so far (paces the commit copy)
-  volatile int* loads_issued = reinterpret_cast<volatile int*>(sgen + SMEM_MISC + 12);
   // the launch's sizes, kept in shared memory (read at item boundaries only,
   // so that they hold no registers through the hot loops)
   Dims* sdims = reinterpret_cast<Dims*>(sgen + SMEM_MISC + 16);
@@ -520,7 +518,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(BAR_MERGE_FREE), 128);
     *abort_flag = 0;
     *issue_lk = 0;
-    *loads_issued = 0;
     *sdims = dims;
     fence_mbar_init();
   }
@@ -554,6 +551,26 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       uint32_t q_phase = 0;
       int issued = 0, q_issued = 0;
       bool ok = true;
+      // Side mode with commit: each side tile is also written to its cache
+      // rows, by two TMA stores (one per 64-column half) from the ring slot
+      // that holds it for the attention.  The producer issues them just
+      // before it refills the slot (the issuers have released it by then,
+      // and it still holds the tile), or at teardown for the last slots, so
+      // no MMA ever waits for a store.  A group's side tiles are spread over
+      // its pair CTAs (tile k's K and V go to pairs (2k) mod P and
+      // (2k + 1) mod P); in a launch of solo CTAs only, each stores its own.
+      uint32_t store_mask = 0;   // ring slots holding a side tile still to store
+      int2* store_info = reinterpret_cast<int2*>(sgen + SMEM_STORE);
+      auto flush_store = [&](uint32_t slot) {
+        const int2 si = store_info[slot];
+        fence_proxy_async_smem();
+        const CUtensorMap* map = (si.y >> 16) ? &tm_vc : &tm_kc;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          tma_store_3d(map, sKV + slot * TILE_BYTES + hf * HALF_BYTES, hf * 64, si.x,
+                       si.y & 0xFFFF);
+        bulk_commit_group();
+      };
       while (ok && iter_next(P, D, it, item)) {
         if (!wait_bar(bar(BAR_Q_EMPTY), q_phase ^ 1u, abort_flag, P.timeout_ns, W_PROD_QE)) break;
         q_phase ^= 1u;
@@ -581,6 +598,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               ok = false;
               break;
             }
+            if ((store_mask >> ring.stage) & 1u) {
+              flush_store(ring.stage);
+              bulk_wait_group_read0();   // the stores have read the slot
+              store_mask &= ~(1u << ring.stage);
+            }
             const uint32_t full = bar(BAR_KV_FULL + ring.stage);
             mbar_arrive_expect_tx(full, TILE_BYTES);
             if (from_side) {
@@ -589,6 +611,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               for (int hf = 0; hf < 2; ++hf)
                 tma_load_2d(sKV + ring.stage * TILE_BYTES + hf * HALF_BYTES, map, full,
                             item.h * HD + hf * 64, kv0);
+              if (P.commit &&
+                  (it.solo ? P.pairs == 0 : (2 * (kv0 / BN) + which) % P.pairs == it.p)) {
+                store_info[ring.stage] = make_int2(P.cache_len + kv0, item.h | (which << 16));
+                store_mask |= 1u << ring.stage;
+              }
             } else {
               const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
               for (int hf = 0; hf < 2; ++hf)
@@ -596,7 +623,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                             kv0, item.h);
             }
             ++issued;
-            *loads_issued = issued;
             ring.advance();
           }
         }
@@ -616,6 +642,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (q_issued > 0)
         wait_bar(bar(BAR_Q_FULL), static_cast<uint32_t>(q_issued - 1) & 1u, &no_abort,
                  DRAIN_TIMEOUT_NS, W_DRAIN_TMA);
+      // the side tiles still held in the ring (now all landed), and every
+      // cache store to completion
+      for (uint32_t slot = 0; slot < ring.n; ++slot)
+        if ((store_mask >> slot) & 1u) flush_store(slot);
+      if (P.commit) bulk_wait_group0();
     }
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
@@ -803,89 +834,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mma_commit(bar(BAR_DRAIN + t));
       volatile int no_abort = 0;
       wait_bar(bar(BAR_DRAIN + t), 0u, &no_abort, DRAIN_TIMEOUT_NS, W_DRAIN_MMA);
-    }
-    __syncwarp();
-  } else if (warp == 11 && P.commit) {
-    // -------------------------------------- store warp (side mode, commit)
-    // Copies the newest block's K/V from the token-major side buffers
-    // ([n_side][H][HD]) into cache rows cache_len + t of every head, in the
-    // background: it takes no part in the K/V ring, so the attention's loads
-    // and MMAs never wait for it.  The 256-byte rows (token t, head h) of
-    // both slices, K then V, are split evenly over the CTAs.  Per iteration
-    // the warp moves 16 consecutive rows: lanes 0-15 the 16-byte columns of
-    // rows r0..r0+7, lanes 16-31 those of rows r0+8..r0+15, 8 loads in flight
-    // per lane before their stores.  The (tensor, t, h) of a lane's first row
-    // takes one division; the next rows step h with a carry, which keeps the
-    // warp's instruction count small (it shares its scheduler with softmax
-    // warps).  No row it writes is read by this launch (the cache maps end at
-    // the history), and the writes are visible once the launch ends.
-    // The copy is paced by the CTA's own progress: iteration k waits until
-    // the producer has issued a matching share of this CTA's K/V loads, so
-    // the copy's HBM traffic is spread thinly over the launch instead of
-    // competing with the loads that fill the pipeline at its start.
-    {
-      constexpr int CPR = HD * 2 / 16;                         // 16-byte chunks per row
-      constexpr int ROWS = 4;
-      const long long per_tensor = static_cast<long long>(P.n_side) * P.heads;
-      const long long total = 2 * per_tensor;
-      const long long r_begin = total * blockIdx.x / gridDim.x;
-      const long long r_end = total * (blockIdx.x + 1) / gridDim.x;
-      const int col = lane & (CPR - 1);
-      const uint4* k_src = static_cast<const uint4*>(P.k_side);
-      const uint4* v_src = static_cast<const uint4*>(P.v_side);
-      uint4* k_dst = reinterpret_cast<uint4*>(P.k_cache);
-      uint4* v_dst = reinterpret_cast<uint4*>(P.v_cache);
-      ItemIter it;
-      iter_init(P, D, it);
-      const long long my_loads = 2 * (it.fe - it.fb);           // unit mode: K and V per key tile
-      const long long iters = (r_end - r_begin + 2 * ROWS - 1) / (2 * ROWS);
-      const long long head = my_loads < NSTAGE ? my_loads : NSTAGE;
-      const uint64_t t_start = global_timer_ns();
-      for (long long r0 = r_begin + ROWS * (lane >> 4); r0 < r_end; r0 += 2 * ROWS) {
-        const long long k = (r0 - r_begin) / (2 * ROWS);
-        const long long target = head + (my_loads - head) * k / iters;
-        bool go = true;
-        while (*loads_issued < target) {
-          if (*abort_flag) { go = false; break; }
-          if (global_timer_ns() - t_start > P.timeout_ns) {
-            *abort_flag = 1;
-            record_error(W_COMMIT);
-            go = false;
-            break;
-          }
-          __nanosleep(256);
-        }
-        if (!go) break;
-        // loads: row r of the slices is row r of K (r < per_tensor) or row
-        // r - per_tensor of V, contiguous in the source
-        uint4 val[ROWS];
-#pragma unroll
-        for (int u = 0; u < ROWS; ++u) {
-          const long long r = r0 + u;
-          if (r < r_end &&
-              WS_BOUND(g_attn_error, (r < per_tensor ? r : r - per_tensor) * CPR + col,
-                       per_tensor * CPR, 27))
-            val[u] = ld_nc_na(r < per_tensor ? k_src + r * CPR + col
-                                             : v_src + (r - per_tensor) * CPR + col);
-        }
-        // stores: (tensor, t, h) of row r0 by one division, then stepped
-        int is_v = r0 >= per_tensor ? 1 : 0;
-        const long long rl = r0 - (is_v ? per_tensor : 0);
-        int t = static_cast<int>(rl / P.heads);
-        int h = static_cast<int>(rl - static_cast<long long>(t) * P.heads);
-#pragma unroll
-        for (int u = 0; u < ROWS; ++u) {
-          if (r0 + u < r_end) {
-            uint4* dst = is_v ? v_dst : k_dst;
-            const long long at = (static_cast<long long>(h) * P.capacity + P.cache_len + t) * CPR + col;
-            if (WS_BOUND(g_attn_error, at, P.heads * P.capacity * CPR, 28)) dst[at] = val[u];
-          }
-          if (++h == P.heads) {
-            h = 0;
-            if (++t == P.n_side) { t = 0; is_v = 1; }
-          }
-        }
-      }
     }
     __syncwarp();
   }
@@ -1364,7 +1312,8 @@ void plan_force_split(TcAttnPlan& p) {
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
-                                const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s) {
+                                const CUtensorMap& tm_vs, const CUtensorMap& tm_kc,
+                                const CUtensorMap& tm_vc, uint64_t timeout_ns, cudaStream_t s) {
   // One-time set-up per device (shared-memory opt-in, register-split check),
   // under a lock so that threads making their first call at once do it once.
   static std::mutex setup_mu;
@@ -1402,10 +1351,6 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   P.cache_len = plan.kv_len - plan.side_len;
   P.n_side = plan.side_len;
   P.commit = (plan.side_len > 0 && a.commit) ? 1 : 0;
-  P.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.k_cache));
-  P.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(a.v_cache));
-  P.k_side = a.k_side;
-  P.v_side = a.v_side;
   P.capacity = a.capacity;
   P.groups = plan.groups;
   P.work = plan.work;
@@ -1426,7 +1371,8 @@ cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
   P.q_max = plan.q_len;
   P.solo = plan.solo;
   P.solo_groups = plan.solo_groups;
-  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs, P);
+  attn_tc_bf16_kernel<<<plan.grid, NUM_THREADS, SMEM_ALLOC, s>>>(tm_q, tm_k, tm_v, tm_ks, tm_vs,
+                                                                 tm_kc, tm_vc, P);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (plan.split) {

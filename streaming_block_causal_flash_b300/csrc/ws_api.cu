@@ -246,6 +246,17 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
     tm_ks = tm_k;    // unused without side buffers
     tm_vs = tm_v;
   }
+  // the commit's store maps: the caches with rows ending at the unit's last
+  // row (cache_len + q_len), so a ragged last side tile is clipped there
+  CUtensorMap tm_kc = tm_k, tm_vc = tm_v;
+  if (side && commit) {
+    cuuint64_t dims[3] = {D, (cuuint64_t)(q_row0 + q_len), (cuuint64_t)num_heads};
+    cuuint64_t strides[2] = {D * 2, (cuuint64_t)capacity * D * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    if (!encode_bf16(&tm_kc, k_cache, 3, dims, strides, box) ||
+        !encode_bf16(&tm_vc, v_cache, 3, dims, strides, box))
+      return fail(WS_ERR_CUDA, "%s: cannot encode the commit tensor maps", who);
+  }
   ws::TcAttnArgs a{};
   a.q = q;
   a.k_cache = k_cache;
@@ -258,9 +269,7 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
   a.workspace = workspace;
   a.force_stall = g_force_stall.load(std::memory_order_relaxed);
   a.commit = (side && commit) ? 1 : 0;
-  a.k_side = k_side;
-  a.v_side = v_side;
-  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs,
+  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_ks, tm_vs, tm_kc, tm_vc,
                                           g_timeout_ns.load(std::memory_order_relaxed), stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();
@@ -544,7 +553,7 @@ ws_status ws_block_causal_attn_dev(const void* q, const void* k_cache, const voi
   a.workspace = workspace;
   a.force_stall = g_force_stall.load(std::memory_order_relaxed);
   a.dev_state = reinterpret_cast<const long long*>(d_state);
-  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_k, tm_v,
+  cudaError_t e = ws::launch_attn_tc_bf16(plan, a, tm_q, tm_k, tm_v, tm_k, tm_v, tm_k, tm_v,
                                           g_timeout_ns.load(std::memory_order_relaxed), stream);
   if (e != cudaSuccess) return cuda_fail(e, who);
   return ok();

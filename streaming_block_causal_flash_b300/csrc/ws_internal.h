@@ -109,8 +109,6 @@ struct TcAttnArgs {
   void* workspace;
   int force_stall;       // test hook (ws_debug_force_wait_timeout)
   int commit;            // side mode: also write the side K/V into the cache
-  const void* k_side;    // side mode: the newest block's K/V, [q_len][H][128] (commit source)
-  const void* v_side;
   // Device-resident unit sizes {cache_len, n_new} (ws_unit_state), read by the
   // kernels at run time; null for host-sized launches.  With it the plan
   // must be made for q_len = the largest unit and kv_len = capacity, with
@@ -120,10 +118,15 @@ struct TcAttnArgs {
 // Forces the split-KV merge and its workspace on (device-resident sizes,
 // where a launch can split any head's key range).
 void plan_force_split(TcAttnPlan& p);
+// tm_kc / tm_vc (side mode with commit): the K/V caches as [H][rows][D]
+// with rows = cache_len + the side length, 128-byte swizzle, box (64, 128, 1):
+// the commit's TMA stores write the side tiles through them, clipped at the
+// unit's last row.  Without commit they are not read.
 cudaError_t launch_attn_tc_bf16(const TcAttnPlan& plan, const TcAttnArgs& a,
                                 const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
-                                const CUtensorMap& tm_vs, uint64_t timeout_ns, cudaStream_t s);
+                                const CUtensorMap& tm_vs, const CUtensorMap& tm_kc,
+                                const CUtensorMap& tm_vc, uint64_t timeout_ns, cudaStream_t s);
 cudaError_t read_attn_device_error(int* code, int* info);
 cudaError_t clear_attn_device_error();
 
