@@ -258,9 +258,6 @@ ws_status run_attention(const char* who, bool prefill, const void* q, const void
       return fail(WS_ERR_CUDA, "%s: cannot encode the commit tensor maps", who);
   }
   ws::TcAttnArgs a{};
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
   a.out = out;
   a.lse = lse;
   a.offs = d_offsets;
@@ -542,9 +539,6 @@ ws_status ws_block_causal_attn_dev(const void* q, const void* k_cache, const voi
       return fail(WS_ERR_CUDA, "%s: cannot encode the K/V tensor maps", who);
   }
   ws::TcAttnArgs a{};
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
   a.out = out;
   a.lse = lse_or_null;
   a.offs = nullptr;

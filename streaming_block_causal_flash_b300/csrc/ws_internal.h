@@ -97,10 +97,8 @@ struct TcAttnPlan {
 bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0, int kv_len,
                   int n_blocks, int num_sms, int side_len = 0, bool allow_solo = true);
 
+// Q, K and V reach the kernel through the tensor maps alone.
 struct TcAttnArgs {
-  const void* q;
-  const void* k_cache;
-  const void* v_cache;
   void* out;
   float* lse;            // may be null
   const int32_t* offs;   // device offsets
