@@ -189,9 +189,12 @@ def test_solver_steps_then_fused_commit():
     assert_close_bf16(plain.float().cpu().numpy(), ref, "after fused commit")
 
 
-def test_side_commit_unit_640x368_matches_append():
-    """At full size the fused commit writes exactly what ws_kv_append writes."""
-    w = WORKLOADS["unit_640x368"]
+@pytest.mark.parametrize("workload", ["unit_640x368", "unit_192x336"])
+def test_side_commit_full_size_matches_append(workload):
+    """At full size the fused commit writes exactly what ws_kv_append writes
+    (640x368: four query-tile pairs per group; 192x336: one pair and solo
+    CTAs for the unpaired third tile, which store nothing)."""
+    w = WORKLOADS[workload]
     sess = bench.UnitSession(w, torch.device("cuda"))
     u = sess.units[0]
     n = sess.sizes[u]
