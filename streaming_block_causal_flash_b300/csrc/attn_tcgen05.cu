@@ -61,9 +61,11 @@
 //    With commit, the side tiles are also written to the cache by TMA
 //    stores from their ring slots (one CTA per group stores), before each
 //    slot is released.
-//  * prefill mode: one work item per (head, query-tile pair), head-major,
-//    longest key range first; key tiles no row of a query tile can see are
-//    skipped; CTAs take items round-robin.
+//  * prefill mode: one work item per (head, query-tile pair); key tiles no
+//    row of a query tile can see are skipped.  CTAs take, round-robin, a
+//    head and a mirrored couple of pairs (z, pairs - 1 - z), which together
+//    cost the same for every couple, so the CTAs move through the heads'
+//    keys together and L2 serves most K/V tiles.
 //
 // Every wait is bounded (wall-clock limit): on time-out the kernel records an
 // error word, stops all roles, waits (bounded) for its own copies and MMAs in
@@ -303,7 +305,8 @@ __device__ __forceinline__ void iter_init(const Params& P, const Dims& D, ItemIt
     }
     it.f = it.fb;
   } else {
-    it.i = blockIdx.x;
+    it.i = blockIdx.x;   // prefill: the couple (see iter_next)
+    it.p = 0;            // 0: the couple's short pair next, 1: its long pair
   }
 }
 
@@ -330,9 +333,26 @@ __device__ __forceinline__ bool iter_next(const Params& P, const Dims& D, ItemIt
     it.f += t1 - t0;
     return true;
   }
-  if (it.i >= P.n_items) return false;
-  item.h = it.i / P.pairs;
-  item.pair = P.pairs - 1 - it.i % P.pairs;   // longest key range first
+  // Prefill: a work unit is a head and a mirrored couple of query-tile
+  // pairs, z and pairs - 1 - z (z < ceil(pairs / 2)), done one after the
+  // other, the short one first.  Pair p sees about 2(p + 1) key tiles, so
+  // every couple costs the same: the CTAs keep step with each other, each
+  // CTA's position in the head's keys stays within a few hundred tiles of
+  // the others', and L2 serves those K/V tiles to all of them.  (Single
+  // pairs dealt longest first let the CTAs spread over whole heads, more
+  // K/V than L2 holds: each tile then left DRAM about 40 times.)
+  const int couples = (P.pairs + 1) / 2;
+  int z, pair;
+  for (;;) {
+    if (it.i >= P.n_items) return false;
+    z = it.i % couples;
+    pair = it.p == 0 ? z : P.pairs - 1 - z;
+    if (it.p == 0 || pair != z) break;
+    it.p = 0;                 // odd pair count: the middle pair has no mirror
+    it.i += gridDim.x;
+  }
+  item.h = it.i / couples;
+  item.pair = pair;
   item.t0 = 0;
   item.slot = -1;
   item.solo = 0;
@@ -346,7 +366,13 @@ __device__ __forceinline__ bool iter_next(const Params& P, const Dims& D, ItemIt
       item.n[t] = 0;
     }
   }
-  it.i += gridDim.x;
+  // next: the couple's mirror, or the next couple
+  if (it.p == 0) {
+    it.p = 1;
+  } else {
+    it.p = 0;
+    it.i += gridDim.x;
+  }
   return true;
 }
 
@@ -1268,7 +1294,8 @@ bool plan_tc_attn(TcAttnPlan& p, bool prefill, int heads, int q_len, int q_row0,
     p.kv_tiles = p.kv_tiles_c + (side_len + BN - 1) / BN;
   }
   if (prefill) {
-    const long long items = static_cast<long long>(heads) * p.pairs;
+    // work units: a head and a mirrored couple of query-tile pairs
+    const long long items = static_cast<long long>(heads) * ((p.pairs + 1) / 2);
     if (items > (1LL << 30)) return false;
     p.n_items = static_cast<int>(items);
     p.grid = p.n_items < num_sms ? p.n_items : num_sms;

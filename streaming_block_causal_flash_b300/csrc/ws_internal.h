@@ -81,7 +81,7 @@ struct TcAttnPlan {
   int kv_tiles;      // ceil(kv_len / 128)
   int groups;        // unit mode: CTA groups over the (head, key tile) space
   int64_t work;      // unit mode: heads * kv_tiles
-  int n_items;       // prefill mode: heads * pairs
+  int n_items;       // prefill mode: heads * ceil(pairs / 2) (mirrored couples of pairs)
   int grid;          // CTAs launched
   bool split;        // unit mode: some head's key range spans several groups
   size_t workspace_bytes;
