@@ -80,6 +80,7 @@ PREFILL_CASES = [
     (14, 2, [700]),                    # one block: full bidirectional attention
     (15, 3, [932] * 3),                # three 640x368-sized units
     (16, 1, [129, 127, 256, 1, 255]),  # straddling tile boundaries
+    (17, 2, [90, 60]),                 # one query-tile pair: a couple of one
 ]
 
 
