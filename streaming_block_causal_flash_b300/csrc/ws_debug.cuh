@@ -10,9 +10,11 @@
 //
 // Check sites (reported by ws_get_device_error): 21 attention output row,
 // 22 attention LSE, 23 split-KV partial write, 24 merge read of a partial,
-// 25 merge output row, 26 merge LSE, 27 fused-commit source, 28 fused-commit
-// cache row, 31 append source, 32 append cache row.  (The Euler kernels index
-// by their loop counters alone, whose loop bounds are the checks.)
+// 25 merge output row, 26 merge LSE, 31 append source, 32 append cache row
+// (27 and 28 are no longer used).  The Euler kernels index by their loop
+// counters alone, whose loop bounds are the checks; TMA copies (the fused
+// commit's stores, the append's tensor store) are clipped by their tensor
+// maps, whose extents end at the rows they may write.
 #pragma once
 
 #ifndef WS_DEBUG
