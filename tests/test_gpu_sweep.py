@@ -3,10 +3,11 @@
 Each case draws a head count and a block layout (history blocks, then the
 query block) from its seed: query blocks of 1 to 9 tiles (odd counts get
 solo CTAs, even ones pairs only), ragged tails, empty history blocks and key
-ranges split over several CTA groups.  Every case runs three ways through the
+ranges split over several CTA groups.  Every case runs five ways through the
 C ABI: the unit call, the side-buffer call with the fused commit (cache rows
-of the unit checked bit for bit, rows past it untouched), and the prefill of
-the whole sequence."""
+of the unit checked bit for bit, rows past it untouched), the call with
+device-resident sizes (a query buffer sized for the largest unit), the
+no-alloc call, and the prefill of the whole sequence."""
 import numpy as np
 import pytest
 import torch
@@ -46,7 +47,7 @@ def draw(seed):
 
 
 @pytest.mark.parametrize("seed", SEEDS)
-def test_random_unit_side_commit_and_prefill(seed):
+def test_random_layout_every_entry_point(seed):
     heads, sizes = draw(seed)
     w = custom_workload(seed, heads, 128)
     case = Case(w, sizes, q_units=[len(sizes) - 1], cap_extra=29)
@@ -88,6 +89,27 @@ def test_random_unit_side_commit_and_prefill(seed):
                              k_side.float().cpu().numpy(), v_side.float().cpu().numpy(), lo)
     ref_s, _ = bc.unit_attention(case.q_host.float().numpy(), k_o, v_o, case.offsets)
     assert_close_bf16(out_s.float().cpu().numpy(), ref_s, f"side+commit {sizes}")
+
+    # device-resident sizes (the graph path): the unit's queries in a buffer
+    # sized for the largest unit, the sizes read from a device state
+    q_max = min(1152, case.cap)        # a unit never exceeds the cache
+    q_buf = torch.zeros(q_max, H, 128, dtype=torch.bfloat16, device="cuda")
+    q_buf[:q_len] = case.q
+    out_d = torch.full_like(q_buf, float("nan"))
+    lse_d = torch.full((H, q_max), float("nan"), device="cuda")
+    wsd = torch.empty(ws.ws_block_causal_attn_dev_workspace_size(q_max, case.cap, H, 128),
+                      dtype=torch.uint8, device="cuda").fill_(0xFF)
+    state = ws.unit_state(lo, q_len, len(sizes) - 1)
+    ws.ws_block_causal_attn_dev(q_buf, case.k, case.v, out_d, state, lse=lse_d, workspace=wsd)
+    torch.cuda.synchronize()
+    assert_close_bf16(out_d[:q_len].float().cpu().numpy(), ref, f"device sizes {sizes}")
+    assert_lse(lse_d[:, :q_len].cpu().numpy(), ref_lse, f"device sizes {sizes}")
+
+    # no-alloc entry point (library scratch instead of a workspace)
+    out_n = torch.full_like(case.q, float("nan"))
+    ws.ws_block_causal_attn_noalloc(case.q, case.k, case.v, out_n, case.offsets, case.offs_dev)
+    torch.cuda.synchronize()
+    assert_close_bf16(out_n.float().cpu().numpy(), ref, f"no-alloc {sizes}")
 
     # prefill of the whole sequence (every block's rows)
     full = Case(w, sizes, cap_extra=3)
