@@ -48,7 +48,9 @@ def _regroup_worker(rank, world, port, q):
     torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
     try:
         out = []
-        for n, H in ((934, 40), (933, 8), (5, 4), (1, 2)):
+        for n, H in ((934, 40), (933, 8), (5, 4), (1, 2), (3, 4)):
+            if H % world:
+                continue                  # heads must divide over the ranks
             g = torch.Generator().manual_seed(n * 100 + H)
             full = torch.randn(n, H, 16, generator=g).to(torch.bfloat16)
             lo, hi = ulysses.shard_bounds(n, world)[rank]
@@ -79,8 +81,10 @@ def _run(worker, world=2, extra=()):
     return dict(res)
 
 
-def test_regrouping_both_directions_bit_exact_two_ranks():
-    res = _run(_regroup_worker)
+@pytest.mark.parametrize("world", [2, 4])
+def test_regrouping_both_directions_bit_exact(world):
+    res = _run(_regroup_worker, world=world)
+    assert len(res) == world
     for rank, rows in res.items():
         for n, H, ok_fwd, ok_back, ok_inv in rows:
             assert ok_fwd, f"rank {rank}: sequence->head differs from slicing (n={n}, H={H})"
@@ -134,9 +138,10 @@ def _step_worker(rank, world, port, q):
         torch.distributed.destroy_process_group()
 
 
-def test_sharded_unit_step_matches_unsharded_two_ranks():
+@pytest.mark.parametrize("world", [2, 4])
+def test_sharded_unit_step_matches_unsharded(world):
     from oracle import block_causal as bc
-    res = _run(_step_worker)
+    res = _run(_step_worker, world=world)
     w = custom_workload(81, HEADS, 128)
     offs = block_offsets(SIZES)
     u = len(SIZES) - 1
